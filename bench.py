@@ -1,0 +1,422 @@
+"""Benchmark of one paged decode step on GB300: slot mapping, KV append and
+paged decode attention (split + combine), all through the libpkv C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha7b]
+    python bench.py --impl reference ...      # the float64 oracle on host cores
+
+Prints one JSON line (rank 0).  The default workload is the Llama-2-7B-shaped
+MHA decode: batch 16, 32 query = 32 KV heads, head_dim 128, fp16, block 16,
+every context 4096 tokens, block tables drawn as a random permutation of a
+4096-block pool.  Its KV cache (1.07 GB read per step) is larger than L2, so
+no flush is needed between steps.  Under torchrun every rank runs its own
+replica of the workload (no data-path collective); the timing is the maximum
+over ranks and ``value`` is the tokens of all ranks divided by it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+# the oracle's numpy/BLAS work is timed on one host thread
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import pkv_workloads as wl  # noqa: E402
+
+METRIC = "decode-attn tokens/s and achieved HBM GB/s (% of GB300 roofline), 1 GPU"
+UNIT = "tokens/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def describe(w: wl.Workload) -> dict:
+    ctx = w.context_lens
+    return {
+        "workload": f"{w.name}: paged decode step, batch {w.batch}, {w.n_q_heads} query / {w.n_kv_heads} KV "
+                    f"heads, head_dim {w.head_dim}, {w.kv_dtype} KV cache, block 16, contexts "
+                    f"{int(ctx.min())}..{int(ctx.max())} (mean {float(ctx.mean()):.0f})",
+        "batch": w.batch, "num_q_heads": w.n_q_heads, "num_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+        "kv_dtype": w.kv_dtype, "block_size": 16, "num_blocks": w.num_blocks,
+        "context_tokens_total": int(ctx.sum()), "partition_tokens": w.partition_tokens,
+        "step": "slot mapping + kv_append + paged decode attention (split + combine)",
+        "l2": f"inputs larger than L2: {w.algorithmic_bytes() / 1e9:.3f} GB of KV + q + out per step, no flush",
+    }
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_153_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("source_digest") != kernel_source_digest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step(w: wl.Workload, seqs) -> int:
+    """One decode step of the float64 oracle for sequences ``seqs``: slot
+    mapping, append, attention for all their query heads.  Returns tokens."""
+    from oracle import attention as oa
+    from oracle import e4m3 as oe
+    from oracle import numerics as on
+    from oracle import slots as osl
+    seqs = list(seqs)
+    slots = osl.slot_mapping(w.block_tables, seqs, w.context_lens[seqs].astype(np.int64) - 1)
+    fp8 = w.kv_dtype == "e4m3"
+    osl.append_rows(w.k_pool, w.k_new[seqs], slots)
+    osl.append_rows(w.v_pool, w.v_new[seqs], slots)
+    q = on.bits_to_f64(w.q[seqs], w.dtype)
+    group = w.n_q_heads // w.n_kv_heads
+    for i, b in enumerate(seqs):
+        n = int(w.context_lens[b])
+        for g in range(w.n_kv_heads):
+            kb = oa.gather_sequence(w.k_pool, w.block_tables[b], n, g)
+            vb = oa.gather_sequence(w.v_pool, w.block_tables[b], n, g)
+            if fp8:
+                keys = oe.decode(oe.encode(wl.bits_to_f32(kb, w.dtype), w.k_scale[g])) * float(w.k_scale[g])
+                values = oe.decode(oe.encode(wl.bits_to_f32(vb, w.dtype), w.v_scale[g])) * float(w.v_scale[g])
+            else:
+                keys, values = on.bits_to_f64(kb, w.kv_dtype), on.bits_to_f64(vb, w.kv_dtype)
+            for h in range(g * group, (g + 1) * group):
+                oa.attend(q[i, h], keys, values, w.scale)
+    return len(seqs)
+
+
+def oracle_sample_size(w: wl.Workload) -> int:
+    return 2 if w.batch >= 2 else 1
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 12.0) -> dict:
+    n = oracle_sample_size(w)
+    done, t0, i = 0, time.perf_counter(), 0
+    while True:
+        seqs = [(i * n + j) % w.batch for j in range(n)]
+        done += oracle_step(w, seqs)
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 4 * w.batch:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} of the workload's sequences ({n} per oracle step, all heads), float64, "
+                      f"{el:.1f} s on one host thread"}
+
+
+def run_reference(args, w: wl.Workload) -> dict:
+    n = oracle_sample_size(w)
+    for i in range(args.warmup):
+        oracle_step(w, [(i * n + j) % w.batch for j in range(n)])
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, [(i * n + j) % w.batch for j in range(n)])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = n * args.steps / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n} sequences (all heads) per step of the same workload, float64 oracle, "
+                                   f"one host thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import paged_kv_cache_153_gb300 as pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    t16 = {"f16": torch.float16, "bf16": torch.bfloat16}
+    stream = torch.cuda.Stream(device=dev)
+    fp8 = w.kv_dtype == "e4m3"
+    with torch.cuda.stream(stream):
+        def up(bits, dt):
+            return torch.from_numpy(np.ascontiguousarray(bits)).view(t16[dt]).to(dev)
+        q, k_new, v_new = up(w.q, w.dtype), up(w.k_new, w.dtype), up(w.v_new, w.dtype)
+        tables = torch.from_numpy(w.block_tables).to(dev)
+        lens = torch.from_numpy(w.context_lens).to(dev)
+        slots = torch.empty(w.batch, dtype=torch.int64, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        max_ctx = int(w.context_lens.max())
+        ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                                        w.max_blocks_per_seq, max_ctx, w.partition_tokens),
+                         dtype=torch.uint8, device=dev)
+        if fp8:
+            nb, H, bs, D = w.k_pool.shape
+            k_cache = torch.empty(nb, H, bs, D, dtype=torch.uint8, device=dev)
+            v_cache = torch.empty_like(k_cache)
+            ks, vs = torch.from_numpy(w.k_scale).to(dev), torch.from_numpy(w.v_scale).to(dev)
+            all_slots = torch.arange(nb * bs, dtype=torch.int64, device=dev)
+            kr = up(w.k_pool, w.dtype).permute(0, 2, 1, 3).reshape(nb * bs, H, D).contiguous()
+            vr = up(w.v_pool, w.dtype).permute(0, 2, 1, 3).reshape(nb * bs, H, D).contiguous()
+            pkv.pkv_kv_append_fp8(kr, vr, all_slots, k_cache, v_cache, ks, vs, err_flag=err, stream=stream)
+            del kr, vr
+        else:
+            k_cache, v_cache = up(w.k_pool, w.kv_dtype), up(w.v_pool, w.kv_dtype)
+        stream.synchronize()
+
+    def attention():
+        if fp8:
+            pkv.pkv_paged_decode_attention_fp8(q, k_cache, v_cache, ks, vs, tables, lens, out, scale=w.scale,
+                                               max_context_len=max_ctx, workspace=ws,
+                                               partition_tokens=w.partition_tokens, err_flag=err,
+                                               stream=stream)
+        else:
+            pkv.pkv_paged_decode_attention(q, k_cache, v_cache, tables, lens, out, scale=w.scale,
+                                           max_context_len=max_ctx, workspace=ws,
+                                           partition_tokens=w.partition_tokens, err_flag=err, stream=stream)
+
+    def step(ev0=None, ev1=None):
+        pkv.pkv_slot_mapping(tables, lens, slots, num_blocks=w.num_blocks, position_offset=-1, err_flag=err,
+                             stream=stream)
+        if fp8:
+            pkv.pkv_kv_append_fp8(k_new, v_new, slots, k_cache, v_cache, ks, vs, err_flag=err, stream=stream)
+        else:
+            pkv.pkv_kv_append(k_new, v_new, slots, k_cache, v_cache, err_flag=err, stream=stream)
+        if ev0 is not None:
+            ev0.record(stream)
+        attention()
+        if ev1 is not None:
+            ev1.record(stream)
+
+    launches_per_step = 4          # slot mapping, append, decode, combine
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    stream.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())} during warm-up")
+
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(*ev_dec[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())} in the timed region")
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # ---- end to end through the host-buffer entry point ---------------------
+    pin = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a)).view(t16[dt]) if dt else
+                              torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
+    e2e = None
+    if not fp8:
+        h_q, h_k, h_v = pin(w.q, w.dtype), pin(w.k_new, w.kv_dtype), pin(w.v_new, w.kv_dtype)
+        h_t, h_l = pin(w.block_tables), pin(w.context_lens)
+        h_out = torch.empty(h_q.shape, dtype=h_q.dtype).pin_memory()
+        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+        d_t, d_l, d_o = torch.empty_like(tables), torch.empty_like(lens), torch.empty_like(out)
+
+        def host_step():
+            pkv.pkv_decode_step_host(h_q, h_k, h_v, h_t, h_l, h_out, d_q, d_k, d_v, d_t, d_l, slots, d_o,
+                                     k_cache, v_cache, scale=w.scale, max_context_len=max_ctx, workspace=ws,
+                                     partition_tokens=w.partition_tokens, err_flag=err, stream=stream)
+            stream.synchronize()           # the result is read on the host every step
+        for _ in range(3):
+            host_step()
+        n_e2e = max(10, min(args.steps, 2000))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        e2e_s = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_t, h_l))
+        e2e = {"value": world * w.batch * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": n_e2e,
+               "path": "pkv_decode_step_host (pinned host buffers in, result read back every step)"}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    algo = w.algorithmic_bytes()
+    achieved = algo / (dec_avg_ms * 1e-3) / 1e9
+    value = world * w.batch * args.steps / (elapsed_ms * 1e-3)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else w.kv_dtype, "data": "synthetic",
+        "config": dict(describe(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+                     "kernel": "pkv_paged_decode_attention call (decode + combine kernels)",
+                     "algorithmic_bytes_per_launch": algo, "avg_launch_ms": dec_avg_ms,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "frac_of_8TBps": achieved / 8000.0},
+        "kv_tokens_per_s": world * int(w.context_lens.sum()) * args.steps / (elapsed_ms * 1e-3),
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = wl.make(args.workload)
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    w = wl.make(args.workload)
+    res = run_gpu(args, w, rank, world, local_rank)
+    if res is not None:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

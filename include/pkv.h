@@ -1,0 +1,216 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode library, libpkv.so.
+ *
+ * What it computes.  A KV cache kept as a pool of fixed-size physical blocks of
+ * 16 tokens; each sequence owns a block table mapping its logical block i to a
+ * physical block ("Series 03: why the KV cache eats memory, and how
+ * PagedAttention pages it", sections 3.1-3.3).  A decode step appends the new
+ * token's K and V rows to the cache and then lets the token's query attend over
+ * every cached row of its sequence ("KV Cache, the memory notepad of LLM
+ * inference", sections 二 and 三):
+ *      out[b, h] = sum_j softmax_j(scale * <q[b, h], K_j>) V_j,   j < context_lens[b]
+ * where K_j / V_j of KV head g = h / G (G = num_q_heads / num_kv_heads, the GQA
+ * group of the same page's section 六) are found through the block table.  An
+ * E4M3 (8-bit float) cache stores code = E4M3(fl32(x / scale[g])) with one fp32
+ * scale per KV head and dequantises before the arithmetic ("KV cache capacity
+ * planning, from the budget to task-level regression", sections 4 and 5).
+ *
+ * Data layout (all row-major, C order):
+ *   k_cache, v_cache   [num_blocks, num_kv_heads, block_size, head_dim]; K and V
+ *                      are separate buffers ("What a KV cache is and why it is
+ *                      the crux of LLM inference", section 3.1); one
+ *                      (block, head) slab of 16 rows is contiguous.
+ *   slot               physical row index = block_id * block_size + offset.
+ *   block_tables       int32 [batch, max_blocks_per_seq]; entries past
+ *                      ceil(context_len / block_size) are never read.
+ *   q, out             [batch, num_q_heads, head_dim] in the 16-bit dtype.
+ *   k_new, v_new       [num_tokens, num_kv_heads, head_dim].
+ *
+ * Conventions.
+ *   - Ownership: every buffer is allocated and owned by the caller.  Device
+ *     pointers must stay valid until the stream work they feed completes.  The
+ *     library allocates no device memory and keeps no device state.
+ *   - Execution: launches are asynchronous on `stream` (a cudaStream_t passed
+ *     as void*; NULL = the legacy default stream).  The returned status only
+ *     reports argument validation and launch errors.
+ *   - Alignment: every device pointer is 16-byte aligned; head_dim is 64 or 128
+ *     and block_size is 16 (anything else returns PKV_ERR_UNSUPPORTED).
+ *   - Device-detected errors (a block id outside [0, num_blocks), a slot past
+ *     the pool, a context longer than its table or than max_context_len, an
+ *     internal wait that timed out) make the kernel skip the access and, when
+ *     `err_flag` (a device int32, nullable) is given, store the first error
+ *     code there.  No kernel traps.  The caller synchronises and reads it.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* bad pointer, size or shape                      */
+  PKV_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, group, block size */
+  PKV_ERR_NO_BLOCKS = 3,    /* the host block pool has no free block            */
+  PKV_ERR_OOB = 4,          /* (device) block id / slot / length out of range   */
+  PKV_ERR_CUDA = 5,         /* a CUDA runtime call failed                        */
+  PKV_ERR_WORKSPACE = 6,    /* workspace missing or smaller than required        */
+  PKV_ERR_TIMEOUT = 7       /* (device) a bounded internal wait expired          */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pkv_version(void);
+
+/* Static text for a status code. */
+const char* pkv_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * Slot mapping.  For token t of sequence b = seq_idx[t] (or b = t when seq_idx
+ * is NULL) at logical position p = positions[t] + position_offset:
+ *     slot_mapping[t] = block_tables[b][p / block_size] * block_size + p % block_size
+ * (the block-table lookup of "Series 03 ...", section 3.1).  p < 0 gives -1 (a
+ * padding token).  A table entry outside [0, num_blocks) or p past the table
+ * gives -1 and PKV_ERR_OOB in err_flag.  Decode: positions = context_lens with
+ * position_offset = -1 (the last position).  All pointers are device memory.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq, int64_t num_blocks,
+                            const int32_t* seq_idx, const int32_t* positions, int32_t position_offset,
+                            int64_t num_tokens, int block_size, int64_t* slot_mapping, int32_t* err_flag,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Append ("KV Cache, the memory notepad ...", section 三: each step appends the
+ * new token's K/V to the cache).  Copies k_new[t, h, :] to
+ * k_cache[s / block_size, h, s % block_size, :] with s = slot_mapping[t], and
+ * the same for V; a bit-exact copy.  s < 0 skips the token; s >= num_blocks *
+ * block_size is skipped and reported as PKV_ERR_OOB.  dtype is the element type
+ * of k_new, v_new and the caches.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t num_tokens,
+                         void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads, int head_dim,
+                         int block_size, pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * E4M3 append ("KV cache capacity planning ...", section 4: FP8 E4M3 storage
+ * with a per-attention-head scale).  Stores
+ *     code = E4M3_RN_satfinite(fl32(x) / k_scale[h])
+ * (IEEE fp32 division, round to nearest even, magnitudes above 448 clamp to
+ * 448) for every element x of k_new (in_dtype) into the uint8 cache, and the
+ * same for V with v_scale.  k_scale, v_scale: device float32 [num_kv_heads].
+ * Slots as in pkv_kv_append.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                             int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                             const float* k_scale, const float* v_scale, int num_kv_heads, int head_dim,
+                             int block_size, pkv_dtype in_dtype, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Workspace for decode attention, in bytes, on the current CUDA device.  The
+ * decode splits the work over the flattened (sequence, KV head, block) space;
+ * pieces of a sequence handled by different thread blocks leave fp32 partial
+ * results (running max, sum, unnormalised output) that a combine kernel merges
+ * by log-sum-exp.  partition_tokens = 0 sizes the balanced split (one equal
+ * share per resident thread block); > 0 (a multiple of block_size) sizes a
+ * split into pieces of that many tokens.  Returns 0 on invalid arguments.
+ * ------------------------------------------------------------------------- */
+size_t pkv_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int max_context_len, int partition_tokens);
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention, 16-bit cache.  For every sequence b and query head h:
+ *     out[b, h] = sum_{j < n} softmax_j(scale * <q[b, h], K_j>) V_j
+ * with n = context_lens[b] and K_j = k_cache[block_tables[b][j / 16], h / G,
+ * j % 16, :] (V likewise).  Softmax arithmetic is fp32 with the running
+ * maximum subtracted; out is rounded to dtype (nearest even).  n = 0 gives
+ * out[b, :, :] = 0.  One thread block serves all G query heads of a KV head,
+ * so each KV byte is read from HBM once.
+ *   q, k_cache, v_cache, out      dtype (F16 / BF16), layouts above.
+ *   block_tables, context_lens    device int32.
+ *   max_context_len               an upper bound of context_lens (sizes the
+ *                                 partition split; longer contexts are clamped
+ *                                 and reported as PKV_ERR_OOB).
+ *   partition_tokens              0 = balanced split; > 0 see the workspace query.
+ *   workspace, workspace_bytes    caller-owned device scratch of at least
+ *                                 pkv_decode_workspace_bytes(...); its contents
+ *                                 need no initialisation and are overwritten.
+ *                                 Two calls running at the same time on the GPU
+ *                                 must not share a workspace.
+ * Requirements: num_q_heads % num_kv_heads == 0 with G in {1, 2, 4, 8};
+ * head_dim in {64, 128}; block_size == 16.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                      float scale, void* out, pkv_dtype dtype, int partition_tokens,
+                                      void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention over an E4M3 cache (uint8 codes) with per-KV-head
+ * scales: K_j and V_j above are replaced by E4M3(code) * k_scale[g] and
+ * E4M3(code) * v_scale[g], dequantised in registers before the arithmetic
+ * ("KV cache capacity planning ...", section 5).  q and out use q_dtype.  All
+ * other arguments as in pkv_paged_decode_attention.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_attention_fp8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                          float scale, void* out, pkv_dtype q_dtype, int partition_tokens,
+                                          void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                          void* stream);
+
+/* ---------------------------------------------------------------------------
+ * One whole decode step from HOST buffers: copies q, k_new, v_new,
+ * block_tables and context_lens from (preferably pinned) host memory into the
+ * caller's device staging buffers, computes the slots of the new tokens
+ * (position context_lens[b] - 1 of sequence b), appends k_new / v_new, runs
+ * paged decode attention and copies out back to host memory, all enqueued on
+ * `stream`.  The caller synchronises the stream before reading h_out.
+ *   h_*        host pointers; shapes as above with num_tokens = batch.
+ *   d_*        device staging buffers of the same sizes; d_slots is int64 [batch].
+ *   caches     device, persistent across steps.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void* h_v_new,
+                                const int32_t* h_block_tables, const int32_t* h_context_lens, void* h_out,
+                                void* d_q, void* d_k_new, void* d_v_new, int32_t* d_block_tables,
+                                int32_t* d_context_lens, int64_t* d_slots, void* d_out, void* k_cache,
+                                void* v_cache, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
+                                size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-side block pool ("Series 03 ...", sections 3.2-3.3; "What a KV cache
+ * is ...", section 3.2): a preallocated set of block ids handed out on demand,
+ * with reference counts for blocks shared by several block tables.  Policy: a
+ * LIFO free list whose first allocations return 0, 1, 2, ...; a block freed by
+ * its last decref is the next one handed out.  Not thread-safe.
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_pool pkv_pool;
+
+/* NULL on invalid arguments or host allocation failure. */
+pkv_pool* pkv_pool_create(int64_t num_blocks, int block_size);
+void pkv_pool_destroy(pkv_pool* pool);
+/* PKV_ERR_NO_BLOCKS when the pool is empty ("What a KV cache is ...", 4.2). */
+pkv_status pkv_pool_alloc(pkv_pool* pool, int32_t* block_id);
+/* PKV_ERR_INVALID_ARG for an id that is not allocated. */
+pkv_status pkv_pool_incref(pkv_pool* pool, int32_t block_id);
+pkv_status pkv_pool_decref(pkv_pool* pool, int32_t block_id);
+int64_t pkv_pool_num_free(const pkv_pool* pool);
+int32_t pkv_pool_refcount(const pkv_pool* pool, int32_t block_id);   /* -1 for a bad id */
+/* Blocks needed for n tokens: ceil(n / block_size) ("Series 03 ...", 3.2). */
+int64_t pkv_blocks_needed(int64_t num_tokens, int block_size);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

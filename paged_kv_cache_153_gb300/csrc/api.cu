@@ -1,0 +1,229 @@
+// C-ABI entry points for decode attention: argument checks, workspace
+// planning and dispatch to the compiled kernel variants.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <mutex>
+
+#include "decode_launch.cuh"
+
+namespace pkv {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == '\0') return fallback;
+  return std::atoi(v);
+}
+
+constexpr int kMaxCtasPerSm = 4;
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t cum_off, ml_off, o_off, total;
+  int64_t slots, ranges_cap;
+};
+
+// Workspace: [B + 1] int32 block-count prefix | [slots, G, 2] fp32 (m, l) |
+// [slots, G, D] fp32 o.  Two partial slots per range of the split.
+bool ws_layout(int batch, int n_kv_heads, int group, int head_dim, int max_blocks_per_seq, int max_context_len,
+               int partition_tokens, int num_sms, WsLayout* w) {
+  if (batch < 0 || n_kv_heads <= 0 || group <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+      max_context_len < 0 || partition_tokens < 0 || num_sms <= 0)
+    return false;
+  if (partition_tokens % kBlockSize) return false;
+  int64_t ranges = static_cast<int64_t>(num_sms) * kMaxCtasPerSm;
+  if (partition_tokens > 0) {
+    const int64_t nblk = std::min<int64_t>(max_blocks_per_seq, (max_context_len + kBlockSize - 1) / kBlockSize);
+    const int64_t w_max = static_cast<int64_t>(batch) * n_kv_heads * nblk;
+    const int64_t pb = partition_tokens / kBlockSize;
+    ranges = std::max<int64_t>((w_max + pb - 1) / pb, 1);
+  }
+  w->ranges_cap = ranges;
+  w->slots = 2 * ranges;
+  w->cum_off = 0;
+  w->ml_off = round256(sizeof(int32_t) * (static_cast<size_t>(batch) + 1));
+  w->o_off = w->ml_off + round256(sizeof(float) * 2 * group * static_cast<size_t>(w->slots));
+  w->total = w->o_off + round256(sizeof(float) * static_cast<size_t>(head_dim) * group * w->slots);
+  return true;
+}
+
+pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                         const float* v_scale, const int32_t* block_tables, const int32_t* context_lens,
+                         int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale, void* out,
+                         pkv_dtype dtype, int partition_tokens, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, void* stream) {
+  if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks < 0 ||
+      max_context_len < 0 || partition_tokens < 0 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (n_q_heads % n_kv_heads) return PKV_ERR_INVALID_ARG;
+  if (partition_tokens % kBlockSize) return PKV_ERR_INVALID_ARG;
+  const int group = n_q_heads / n_kv_heads;
+  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+    return PKV_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+    return PKV_ERR_INVALID_ARG;
+  const int num_sms = sm_count();
+  if (num_sms <= 0) return PKV_ERR_CUDA;
+  WsLayout w;
+  if (!ws_layout(batch, n_kv_heads, group, head_dim, max_blocks_per_seq, max_context_len, partition_tokens,
+                 num_sms, &w))
+    return PKV_ERR_INVALID_ARG;
+  if (workspace_bytes < w.total) return PKV_ERR_WORKSPACE;
+  if (w.slots > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+
+  DecodeLauncher launch = fp8 ? decode_launcher_e4m3(dtype, head_dim, group)
+                              : (dtype == PKV_F16 ? decode_launcher_f16(head_dim, group)
+                                                  : decode_launcher_bf16(head_dim, group));
+  if (launch == nullptr) return PKV_ERR_UNSUPPORTED;
+
+  char* ws = static_cast<char*>(workspace);
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_cum = reinterpret_cast<int32_t*>(ws + w.cum_off);
+  p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
+  p.err = err_flag;
+  p.num_blocks = num_blocks;
+  p.batch = batch;
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_nblk = (max_context_len + kBlockSize - 1) / kBlockSize;
+  p.part_blocks = partition_tokens / kBlockSize;
+  p.slot_capacity = static_cast<int>(w.slots);
+  p.qk_scale_log2 = scale * kLog2e;
+
+  LaunchInfo li{};
+  li.num_sms = num_sms;
+  li.max_ctas_per_sm = std::max(1, std::min(kMaxCtasPerSm, env_int("PKV_CTAS_PER_SM", kMaxCtasPerSm)));
+  li.stages = env_int("PKV_STAGES", 0);
+  li.part_ranges_cap = w.ranges_cap;
+  return launch(p, li, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_version(void) { return 100; }
+
+extern "C" const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_NO_BLOCKS: return "no free block in the pool";
+    case PKV_ERR_OOB: return "block id, slot or context length out of range";
+    case PKV_ERR_CUDA: return "CUDA runtime error";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_TIMEOUT: return "an internal device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" size_t pkv_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                             int max_blocks_per_seq, int max_context_len, int partition_tokens) {
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  const int num_sms = sm_count();
+  if (num_sms <= 0) return 0;
+  WsLayout w;
+  if (!ws_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, max_blocks_per_seq, max_context_len,
+                 partition_tokens, num_sms, &w))
+    return 0;
+  return w.total;
+}
+
+extern "C" pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                                 const int32_t* block_tables, const int32_t* context_lens,
+                                                 int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                                 int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                                 int max_context_len, float scale, void* out, pkv_dtype dtype,
+                                                 int partition_tokens, void* workspace, size_t workspace_bytes,
+                                                 int32_t* err_flag, void* stream) {
+  return decode_common(false, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       max_context_len, scale, out, dtype, partition_tokens, workspace, workspace_bytes, err_flag,
+                       stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_attention_fp8(const void* q, const uint8_t* k_cache,
+                                                     const uint8_t* v_cache, const float* k_scale,
+                                                     const float* v_scale, const int32_t* block_tables,
+                                                     const int32_t* context_lens, int batch, int num_q_heads,
+                                                     int num_kv_heads, int head_dim, int block_size,
+                                                     int max_blocks_per_seq, int64_t num_blocks,
+                                                     int max_context_len, float scale, void* out,
+                                                     pkv_dtype q_dtype, int partition_tokens, void* workspace,
+                                                     size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return decode_common(true, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       max_context_len, scale, out, q_dtype, partition_tokens, workspace, workspace_bytes,
+                       err_flag, stream);
+}
+
+extern "C" pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void* h_v_new,
+                                           const int32_t* h_block_tables, const int32_t* h_context_lens,
+                                           void* h_out, void* d_q, void* d_k_new, void* d_v_new,
+                                           int32_t* d_block_tables, int32_t* d_context_lens, int64_t* d_slots,
+                                           void* d_out, void* k_cache, void* v_cache, int batch,
+                                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                           int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                           float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
+                                           size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!h_q || !h_k_new || !h_v_new || !h_block_tables || !h_context_lens || !h_out || !d_q || !d_k_new ||
+      !d_v_new || !d_block_tables || !d_context_lens || !d_slots || !d_out)
+    return PKV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qo_bytes = static_cast<size_t>(batch) * num_q_heads * head_dim * 2;
+  const size_t kv_bytes = static_cast<size_t>(batch) * num_kv_heads * head_dim * 2;
+  const size_t tab_bytes = static_cast<size_t>(batch) * max_blocks_per_seq * sizeof(int32_t);
+  if (cudaMemcpyAsync(d_q, h_q, qo_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_k_new, h_k_new, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_v_new, h_v_new, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_block_tables, h_block_tables, tab_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_context_lens, h_context_lens, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+    return PKV_ERR_CUDA;
+  pkv_status st = pkv_slot_mapping(d_block_tables, max_blocks_per_seq, num_blocks, nullptr, d_context_lens, -1,
+                                   batch, block_size, d_slots, err_flag, stream);
+  if (st != PKV_OK) return st;
+  st = pkv_kv_append(d_k_new, d_v_new, d_slots, batch, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
+                     block_size, dtype, err_flag, stream);
+  if (st != PKV_OK) return st;
+  st = pkv_paged_decode_attention(d_q, k_cache, v_cache, d_block_tables, d_context_lens, batch, num_q_heads,
+                                  num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                  max_context_len, scale, d_out, dtype, partition_tokens, workspace,
+                                  workspace_bytes, err_flag, stream);
+  if (st != PKV_OK) return st;
+  if (cudaMemcpyAsync(h_out, d_out, qo_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}

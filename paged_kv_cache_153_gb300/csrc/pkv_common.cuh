@@ -1,0 +1,197 @@
+// Device-side helpers shared by the paged KV-cache kernels (sm_103a).
+//
+// * mbarrier / 1-D bulk-copy (TMA) wrappers in inline PTX.  Every wait is
+//   bounded by the global timer: a wait that runs past kWaitLimitNs records
+//   PKV_ERR_TIMEOUT in the caller's error word and returns false, so no kernel
+//   here can spin forever.
+// * 16-bit / E4M3 -> fp32 conversions and the fp32 -> 16-bit output rounding.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;                       // tokens per physical block
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// error word: the first error code wins; later ones are dropped
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void record_error(int32_t* err, int code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses and mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// make the initialised barriers visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (and
+// records PKV_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      record_error(err, PKV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// L2 policy for data read exactly once (private KV blocks)
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes must be a
+// multiple of 16 and both addresses 16-byte aligned)
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// named barrier among a subset of warps (id 0 is __syncthreads)
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// named barrier that also ORs a predicate over the participating threads, so
+// every participant takes the same decision
+__device__ __forceinline__ bool named_bar_red_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, "
+      "q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// Wait for a phase until an absolute global-timer deadline (used when draining
+// copies before exit); returns false on expiry without recording an error.
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned long long deadline) {
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() > deadline) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// element conversions
+// ---------------------------------------------------------------------------
+struct F16 {
+  using storage = __half;
+  static constexpr int kBytes = 2;
+};
+struct BF16 {
+  using storage = __nv_bfloat16;
+  static constexpr int kBytes = 2;
+};
+struct E4M3 {
+  using storage = uint8_t;
+  static constexpr int kBytes = 1;
+};
+
+// two packed 16-bit values -> two floats
+__device__ __forceinline__ float2 unpack2(uint32_t w, F16) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+__device__ __forceinline__ float2 unpack2(uint32_t w, BF16) {
+  // bf16 is the upper half of an fp32: shifting is an exact conversion
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// two packed E4M3 codes (low byte first) -> two floats, exactly
+__device__ __forceinline__ float2 unpack2_e4m3(uint16_t w) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(w));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// 8 consecutive elements of a row -> 8 floats
+__device__ __forceinline__ void load8(const void* p, float* f, F16) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  float2 a = unpack2(v.x, F16{}), b = unpack2(v.y, F16{}), c = unpack2(v.z, F16{}), d = unpack2(v.w, F16{});
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+__device__ __forceinline__ void load8(const void* p, float* f, BF16) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  float2 a = unpack2(v.x, BF16{}), b = unpack2(v.y, BF16{}), c = unpack2(v.z, BF16{}), d = unpack2(v.w, BF16{});
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+__device__ __forceinline__ void load8(const void* p, float* f, E4M3) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  float2 a = unpack2_e4m3(static_cast<uint16_t>(v.x & 0xffffu));
+  float2 b = unpack2_e4m3(static_cast<uint16_t>(v.x >> 16));
+  float2 c = unpack2_e4m3(static_cast<uint16_t>(v.y & 0xffffu));
+  float2 d = unpack2_e4m3(static_cast<uint16_t>(v.y >> 16));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+// fp32 -> output element, round to nearest even
+__device__ __forceinline__ __half to_out(float x, F16) { return __float2half_rn(x); }
+__device__ __forceinline__ __nv_bfloat16 to_out(float x, BF16) { return __float2bfloat16_rn(x); }
+
+}  // namespace pkv

@@ -112,7 +112,17 @@ def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def _normal_bits(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
-    return f32_to_bits(rng.standard_normal(shape, dtype=np.float32), dtype)
+    """N(0, 1) draws rounded to ``dtype``, generated in chunks of the flat
+    array so that no full-size float32 temporary is needed."""
+    out = np.empty(shape, dtype=np.uint16)
+    flat = out.reshape(-1)
+    chunk = 1 << 22
+    buf = np.empty(chunk, dtype=np.float32)
+    for s in range(0, flat.size, chunk):
+        n = min(chunk, flat.size - s)
+        rng.standard_normal(out=buf[:n], dtype=np.float32)
+        flat[s:s + n] = f32_to_bits(buf[:n], dtype)
+    return out
 
 
 def _bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:

@@ -1,0 +1,175 @@
+"""Helpers for the GPU parity tests: move a seeded workload to the device,
+run the CUDA path through the C ABI, and build the oracle's expectation.
+
+Nothing here computes the method on the GPU side except through libpkv.so;
+the expectations come only from ``oracle``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import pkv_workloads as wl
+from oracle import attention as oa
+from oracle import e4m3 as oe
+from oracle import numerics as on
+from oracle import slots as osl
+
+ATOL, RTOL = 2e-3, 1e-2          # fp16 / bf16 attention: |gpu - ref| <= ATOL + RTOL |ref|
+FP8_ATOL = 2e-2                  # E4M3 attention: |gpu - ref| <= FP8_ATOL (same codes on both sides)
+
+TORCH_16 = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def bits_to_torch(bits: np.ndarray, dtype: str, device=None) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits)).view(TORCH_16[dtype])
+    return t.to(device or dev())
+
+
+def torch_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().view(torch.uint16).numpy() if t.dtype != torch.uint8 else t.cpu().numpy()
+
+
+class GpuCase:
+    """Device copies of a workload plus the buffers one decode step needs."""
+
+    def __init__(self, w: wl.Workload, *, codes=None, max_context_len=None):
+        d = dev()
+        self.w = w
+        self.fp8 = w.kv_dtype == "e4m3"
+        if self.fp8:
+            kc, vc = codes
+            self.k_cache = torch.from_numpy(kc).to(d)
+            self.v_cache = torch.from_numpy(vc).to(d)
+            self.k_scale = torch.from_numpy(w.k_scale).to(d)
+            self.v_scale = torch.from_numpy(w.v_scale).to(d)
+        else:
+            self.k_cache = bits_to_torch(w.k_pool, w.kv_dtype)
+            self.v_cache = bits_to_torch(w.v_pool, w.kv_dtype)
+        self.q = bits_to_torch(w.q, w.dtype)
+        self.k_new = bits_to_torch(w.k_new, w.dtype if self.fp8 else w.kv_dtype)
+        self.v_new = bits_to_torch(w.v_new, w.dtype if self.fp8 else w.kv_dtype)
+        self.tables = torch.from_numpy(w.block_tables).to(d)
+        self.lens = torch.from_numpy(w.context_lens).to(d)
+        self.slots = torch.empty(w.batch, dtype=torch.int64, device=d)
+        self.out = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=d)
+        self.max_ctx = int(max_context_len if max_context_len is not None else max(1, w.context_lens.max()))
+        self.ws = None
+
+    def workspace(self, partition_tokens):
+        import paged_kv_cache_153_gb300 as pkv
+        w = self.w
+        n = pkv.pkv_decode_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                           w.max_blocks_per_seq, self.max_ctx, partition_tokens)
+        if self.ws is None or self.ws.numel() < n:
+            self.ws = torch.empty(n, dtype=torch.uint8, device=dev())
+        return self.ws
+
+    def step(self, partition_tokens=None, append=True, stream=None):
+        """slot mapping + append + decode attention, all through the C ABI."""
+        import paged_kv_cache_153_gb300 as pkv
+        w = self.w
+        pt = w.partition_tokens if partition_tokens is None else partition_tokens
+        ws = self.workspace(pt)
+        if append:
+            pkv.pkv_slot_mapping(self.tables, self.lens, self.slots, num_blocks=w.num_blocks,
+                                 position_offset=-1, err_flag=self.err, stream=stream)
+            if self.fp8:
+                pkv.pkv_kv_append_fp8(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
+                                      self.k_scale, self.v_scale, err_flag=self.err, stream=stream)
+            else:
+                pkv.pkv_kv_append(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
+                                  err_flag=self.err, stream=stream)
+        if self.fp8:
+            pkv.pkv_paged_decode_attention_fp8(self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                                               self.tables, self.lens, self.out, scale=w.scale,
+                                               max_context_len=self.max_ctx, workspace=ws,
+                                               partition_tokens=pt, err_flag=self.err, stream=stream)
+        else:
+            pkv.pkv_paged_decode_attention(self.q, self.k_cache, self.v_cache, self.tables, self.lens,
+                                           self.out, scale=w.scale, max_context_len=self.max_ctx,
+                                           workspace=ws, partition_tokens=pt, err_flag=self.err,
+                                           stream=stream)
+        return self.out
+
+    def err_code(self) -> int:
+        torch.cuda.synchronize()
+        return int(self.err.item())
+
+
+# ---------------------------------------------------------------------------
+# oracle side
+# ---------------------------------------------------------------------------
+def oracle_slots(w: wl.Workload) -> np.ndarray:
+    return osl.slot_mapping(w.block_tables, range(w.batch), w.context_lens.astype(np.int64) - 1)
+
+
+def oracle_pools_after_append(w: wl.Workload):
+    """Bit patterns (16-bit) or E4M3 codes of the pools after the step's append."""
+    slots = oracle_slots(w)
+    if w.kv_dtype == "e4m3":
+        kc, vc, kn, vn = oracle_fp8_codes(w)
+        osl.append_rows(kc, kn, slots)
+        osl.append_rows(vc, vn, slots)
+        return kc, vc
+    kp, vp = w.k_pool.copy(), w.v_pool.copy()
+    osl.append_rows(kp, w.k_new, slots)
+    osl.append_rows(vp, w.v_new, slots)
+    return kp, vp
+
+
+def oracle_fp8_codes(w: wl.Workload):
+    """Oracle E4M3 codes of the whole pool (before the append) and of the new
+    rows, per KV head with that head's scale."""
+    kc = np.empty(w.k_pool.shape, dtype=np.uint8)
+    vc = np.empty(w.v_pool.shape, dtype=np.uint8)
+    kn = np.empty(w.k_new.shape, dtype=np.uint8)
+    vn = np.empty(w.v_new.shape, dtype=np.uint8)
+    for g in range(w.n_kv_heads):
+        kc[:, g] = oe.encode(wl.bits_to_f32(w.k_pool[:, g], w.dtype), w.k_scale[g])
+        vc[:, g] = oe.encode(wl.bits_to_f32(w.v_pool[:, g], w.dtype), w.v_scale[g])
+        kn[:, g] = oe.encode(wl.bits_to_f32(w.k_new[:, g], w.dtype), w.k_scale[g])
+        vn[:, g] = oe.encode(wl.bits_to_f32(w.v_new[:, g], w.dtype), w.v_scale[g])
+    return kc, vc, kn, vn
+
+
+def oracle_decode(w: wl.Workload, kp, vp, pairs=None):
+    """float64 expectation for (b, h) pairs (all pairs when None); kp/vp are
+    16-bit bit patterns or (for E4M3) codes of the pools after the append."""
+    q = on.bits_to_f64(w.q, w.dtype)
+    group = w.n_q_heads // w.n_kv_heads
+    if pairs is None:
+        pairs = [(b, h) for b in range(w.batch) for h in range(w.n_q_heads)]
+    out = {}
+    for b, h in pairs:
+        g = h // group
+        n = int(w.context_lens[b])
+        kb = oa.gather_sequence(kp, w.block_tables[b], n, g)
+        vb = oa.gather_sequence(vp, w.block_tables[b], n, g)
+        if w.kv_dtype == "e4m3":
+            keys = oe.decode(kb) * float(w.k_scale[g])
+            values = oe.decode(vb) * float(w.v_scale[g])
+        else:
+            keys = on.bits_to_f64(kb, w.kv_dtype)
+            values = on.bits_to_f64(vb, w.kv_dtype)
+        out[(b, h)] = oa.attend(q[b, h], keys, values, w.scale)
+    return out
+
+
+def compare(got: torch.Tensor, ref: dict, fp8: bool = False):
+    """Elementwise tolerance check; returns (max_abs, max_rel, n_bad)."""
+    g = got.float().cpu().numpy().astype(np.float64)
+    max_abs = max_rel = 0.0
+    n_bad = 0
+    for (b, h), r in ref.items():
+        diff = np.abs(g[b, h] - r)
+        lim = FP8_ATOL if fp8 else ATOL + RTOL * np.abs(r)
+        n_bad += int((diff > lim).sum())
+        max_abs = max(max_abs, float(diff.max()))
+        max_rel = max(max_rel, float((diff / np.maximum(np.abs(r), 1e-30)).max()))
+    return max_abs, max_rel, n_bad

@@ -1,0 +1,108 @@
+"""CPU-only checks of the C ABI: every declared symbol is exported, argument
+validation that returns before any CUDA call, and the host block pool against
+the oracle's pool."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.block_pool import BlockPool as OraclePool, PoolExhausted, blocks_needed
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import __graft_entry__ as g
+    g.build()
+    import paged_kv_cache_153_gb300 as m
+    return m
+
+
+def declared_symbols():
+    names = set()
+    for fname in os.listdir(os.path.join(ROOT, "include")):
+        if fname.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fname)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(pkv):
+    names = declared_symbols()
+    assert {"pkv_kv_append", "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8"} <= names
+    lib = C.CDLL(pkv.library_path)
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(pkv):
+    assert pkv.pkv_status_string(0) == "ok"
+    assert "workspace" in pkv.pkv_status_string(6)
+    assert pkv.pkv_version() >= 100
+
+
+def test_validation_before_any_cuda_call(pkv):
+    lib = pkv.lib
+    dummy = C.c_void_p(16)
+    # group 3 is not built
+    st = lib.pkv_paged_decode_attention(dummy, dummy, dummy, dummy, dummy, 2, 6, 2, 128, 16, 4, 8, 64,
+                                        0.1, dummy, 0, 0, dummy, 1 << 20, None, None)
+    assert st == 2
+    # H_q not a multiple of H_kv
+    st = lib.pkv_paged_decode_attention(dummy, dummy, dummy, dummy, dummy, 2, 5, 2, 128, 16, 4, 8, 64,
+                                        0.1, dummy, 0, 0, dummy, 1 << 20, None, None)
+    assert st == 1
+    # block size other than 16, head_dim 96
+    assert lib.pkv_kv_append(dummy, dummy, dummy, 1, dummy, dummy, 4, 2, 128, 32, 0, None, None) == 2
+    assert lib.pkv_kv_append(dummy, dummy, dummy, 1, dummy, dummy, 4, 2, 96, 16, 0, None, None) == 2
+    # partition not a multiple of the block size
+    st = lib.pkv_paged_decode_attention(dummy, dummy, dummy, dummy, dummy, 2, 4, 2, 128, 16, 4, 8, 64,
+                                        0.1, dummy, 0, 24, dummy, 1 << 20, None, None)
+    assert st == 1
+    # empty work is a no-op
+    assert lib.pkv_kv_append(None, None, None, 0, None, None, 4, 2, 128, 16, 0, None, None) == 0
+    # null pointers with work
+    assert lib.pkv_kv_append(None, dummy, dummy, 1, dummy, dummy, 4, 2, 128, 16, 0, None, None) == 1
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_host_pool_matches_oracle_pool(pkv, seed):
+    rng = np.random.default_rng(seed)
+    n = 37
+    ours, ref = pkv.BlockPool(n), OraclePool(n)
+    held = []
+    for _ in range(600):
+        op = rng.integers(3)
+        if op == 0:
+            try:
+                b = ref.alloc()
+            except PoolExhausted:
+                with pytest.raises(pkv.PkvError) as ei:
+                    ours.alloc()
+                assert ei.value.status == 3
+                continue
+            assert ours.alloc() == b
+            held.append(b)
+        elif op == 1 and held:
+            b = held[rng.integers(len(held))]
+            ref.incref(b)
+            ours.incref(b)
+            held.append(b)
+        elif op == 2 and held:
+            b = held.pop(rng.integers(len(held)))
+            ref.decref(b)
+            ours.decref(b)
+        assert ours.num_free == ref.num_free
+    for b in range(n):
+        assert ours.refcount(b) == ref.refcount(b)
+    with pytest.raises(pkv.PkvError):
+        ours.incref(n + 5)
+
+
+def test_blocks_needed(pkv):
+    for t in [0, 1, 15, 16, 17, 1200, 65536]:
+        assert pkv.pkv_blocks_needed(t) == blocks_needed(t)
