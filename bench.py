@@ -40,6 +40,14 @@ UNIT = "tokens/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
 
+_T0 = time.perf_counter()
+
+
+def log(msg: str) -> None:
+    """Progress on stderr (the JSON result is the only line on stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+
+
 def describe(w: wl.Workload) -> dict:
     ctx = w.context_lens
     return {
@@ -225,6 +233,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     import __graft_entry__ as ge
     ge.build()
     import paged_kv_cache_153_gb300 as pkv
+    log("library ready")
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -257,6 +266,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         else:
             k_cache, v_cache = up(w.k_pool, w.kv_dtype), up(w.v_pool, w.kv_dtype)
         stream.synchronize()
+    log("inputs resident on the device")
 
     def attention():
         if fp8:
@@ -293,11 +303,15 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         if dist is not None:
             dist.barrier()
 
-    for _ in range(max(args.warmup, 3)):
+    for i in range(max(args.warmup, 3)):
         step()
+        if i == 0:
+            stream.synchronize()
+            log(f"first step done, device error word {int(err.item())}")
     stream.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error {int(err.item())} during warm-up")
+    log("warm-up done")
 
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
@@ -312,6 +326,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         torch.cuda.synchronize(dev)
         barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
+    log(f"timed region done: {elapsed_ms / args.steps:.4f} ms per step")
     if int(err.item()) != 0:
         raise RuntimeError(f"device error {int(err.item())} in the timed region")
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
@@ -349,6 +364,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
             t = torch.tensor([e2e_s], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_s = float(t.item())
+        log("end-to-end loop done")
         h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_t, h_l))
         e2e = {"value": world * w.batch * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": n_e2e,
@@ -407,6 +423,7 @@ def main():
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
     w = wl.make(args.workload)
+    log(f"workload {w.name} generated")
     res = run_gpu(args, w, rank, world, local_rank)
     if res is not None:
         if world == 1 and not args.no_cpu_baseline:

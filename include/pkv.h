@@ -70,6 +70,10 @@ int pkv_version(void);
 /* Static text for a status code. */
 const char* pkv_status_string(int status);
 
+/* The CUDA runtime call that made the calling thread's last PKV_ERR_CUDA
+ * (name, error name and text); "" when none has failed.  Thread-local. */
+const char* pkv_last_error(void);
+
 /* ---------------------------------------------------------------------------
  * Slot mapping.  For token t of sequence b = seq_idx[t] (or b = t when seq_idx
  * is NULL) at logical position p = positions[t] + position_offset:

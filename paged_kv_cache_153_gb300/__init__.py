@@ -20,7 +20,7 @@ __all__ = [
     "PKV_F16", "PKV_BF16", "PkvError", "lib", "library_path",
     "pkv_slot_mapping", "pkv_kv_append", "pkv_kv_append_fp8", "pkv_decode_workspace_bytes",
     "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8", "pkv_decode_step_host",
-    "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string",
+    "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
 ]
 
 PKV_F16 = 0
@@ -37,6 +37,7 @@ _p, _i, _i64, _sz, _f = C.c_void_p, C.c_int, C.c_int64, C.c_size_t, C.c_float
 _SIGS = {
     "pkv_version": (_i, []),
     "pkv_status_string": (C.c_char_p, [_i]),
+    "pkv_last_error": (C.c_char_p, []),
     "pkv_slot_mapping": (_i, [_p, _i, _i64, _p, _p, C.c_int32, _i64, _i, _p, _p, _p]),
     "pkv_kv_append": (_i, [_p, _p, _p, _i64, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
     "pkv_kv_append_fp8": (_i, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i, _i, _i, _i, _p, _p]),
@@ -64,7 +65,8 @@ for _name, (_res, _args) in _SIGS.items():
 
 class PkvError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn}: {pkv_status_string(status)} (status {status})")
+        detail = f": {pkv_last_error()}" if status == 5 else ""
+        super().__init__(f"{fn}: {pkv_status_string(status)} (status {status}){detail}")
         self.status = status
 
 
@@ -74,6 +76,10 @@ def pkv_version() -> int:
 
 def pkv_status_string(status: int) -> str:
     return lib.pkv_status_string(status).decode()
+
+
+def pkv_last_error() -> str:
+    return lib.pkv_last_error().decode()
 
 
 def _check(fn: str, status: int) -> None:

@@ -7,8 +7,25 @@
 #include <mutex>
 
 #include "decode_launch.cuh"
+#include "host_util.h"
+
+#include <cstdio>
+#include <cstring>
 
 namespace pkv {
+
+namespace {
+thread_local char g_last_error[256] = "";
+}
+
+bool cuda_failed(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return false;
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  cudaGetLastError();   // clear the non-sticky error state
+  return true;
+}
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -23,8 +40,9 @@ constexpr int kMaxCtasPerSm = 4;
 
 int sm_count() {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cuda_failed(cudaGetDevice(&dev), "cudaGetDevice")) return 0;
+  if (cuda_failed(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"))
+    return 0;
   return n;
 }
 
@@ -133,6 +151,8 @@ using namespace pkv;
 
 extern "C" int pkv_version(void) { return 100; }
 
+extern "C" const char* pkv_last_error(void) { return g_last_error; }
+
 extern "C" const char* pkv_status_string(int status) {
   switch (status) {
     case PKV_OK: return "ok";
@@ -206,12 +226,14 @@ extern "C" pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new,
   const size_t qo_bytes = static_cast<size_t>(batch) * num_q_heads * head_dim * 2;
   const size_t kv_bytes = static_cast<size_t>(batch) * num_kv_heads * head_dim * 2;
   const size_t tab_bytes = static_cast<size_t>(batch) * max_blocks_per_seq * sizeof(int32_t);
-  if (cudaMemcpyAsync(d_q, h_q, qo_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_k_new, h_k_new, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_v_new, h_v_new, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_block_tables, h_block_tables, tab_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_context_lens, h_context_lens, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s) !=
-          cudaSuccess)
+  if (cuda_failed(cudaMemcpyAsync(d_q, h_q, qo_bytes, cudaMemcpyHostToDevice, s), "cudaMemcpyAsync q") ||
+      cuda_failed(cudaMemcpyAsync(d_k_new, h_k_new, kv_bytes, cudaMemcpyHostToDevice, s), "cudaMemcpyAsync k") ||
+      cuda_failed(cudaMemcpyAsync(d_v_new, h_v_new, kv_bytes, cudaMemcpyHostToDevice, s), "cudaMemcpyAsync v") ||
+      cuda_failed(cudaMemcpyAsync(d_block_tables, h_block_tables, tab_bytes, cudaMemcpyHostToDevice, s),
+                  "cudaMemcpyAsync tables") ||
+      cuda_failed(cudaMemcpyAsync(d_context_lens, h_context_lens, sizeof(int32_t) * batch,
+                                  cudaMemcpyHostToDevice, s),
+                  "cudaMemcpyAsync lens"))
     return PKV_ERR_CUDA;
   pkv_status st = pkv_slot_mapping(d_block_tables, max_blocks_per_seq, num_blocks, nullptr, d_context_lens, -1,
                                    batch, block_size, d_slots, err_flag, stream);
@@ -224,6 +246,7 @@ extern "C" pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new,
                                   max_context_len, scale, d_out, dtype, partition_tokens, workspace,
                                   workspace_bytes, err_flag, stream);
   if (st != PKV_OK) return st;
-  if (cudaMemcpyAsync(h_out, d_out, qo_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cuda_failed(cudaMemcpyAsync(h_out, d_out, qo_bytes, cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync out"))
+    return PKV_ERR_CUDA;
   return PKV_OK;
 }

@@ -8,6 +8,7 @@
 // E4M3_RN_satfinite(fl32(x) / scale[h]).
 #include <cuda_runtime.h>
 
+#include "host_util.h"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -121,8 +122,8 @@ using namespace pkv;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static pkv_status launch_status() {
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+static pkv_status launch_status(const char* what) {
+  return cuda_failed(cudaGetLastError(), what) ? PKV_ERR_CUDA : PKV_OK;
 }
 
 extern "C" pkv_status pkv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq, int64_t num_blocks,
@@ -138,7 +139,7 @@ extern "C" pkv_status pkv_slot_mapping(const int32_t* block_tables, int max_bloc
   slot_mapping_kernel<<<static_cast<unsigned>(grid), threads, 0, static_cast<cudaStream_t>(stream)>>>(
       block_tables, max_blocks_per_seq, num_blocks, seq_idx, positions, position_offset, num_tokens,
       slot_mapping, err_flag);
-  return launch_status();
+  return launch_status("slot_mapping_kernel launch");
 }
 
 extern "C" pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -160,7 +161,7 @@ extern "C" pkv_status pkv_kv_append(const void* k_new, const void* v_new, const 
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks * kBlockSize, num_kv_heads, chunks,
       err_flag);
-  return launch_status();
+  return launch_status("kv_append_kernel launch");
 }
 
 extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -191,5 +192,5 @@ extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, co
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
         reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale, v_scale,
         num_blocks * kBlockSize, num_kv_heads, chunks, err_flag);
-  return launch_status();
+  return launch_status("kv_append_fp8_kernel launch");
 }

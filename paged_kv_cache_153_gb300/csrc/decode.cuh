@@ -331,8 +331,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       const uint32_t first = k > static_cast<uint32_t>(S) ? k - S : 0;
       for (uint32_t kk = first; kk < k; ++kk)
         if (stage_ok[kk % S]) mbar_wait_until(&full_bar[kk % S], (kk / S) & 1, deadline);
-      for (uint32_t jj = (j > 2 ? j - 2 : 0); jj < j; ++jj)
-        mbar_wait_until(&qfull_bar[jj & 1], (jj >> 1) & 1, deadline);
+      // Only the last segment's query copy can still be in flight: the one
+      // before it shares its slot with the end marker, whose publication
+      // waited until the consumers had read that copy (and re-armed the slot).
+      if (j >= 1) mbar_wait_until(&qfull_bar[(j - 1) & 1], ((j - 1) >> 1) & 1, deadline);
     }
     __syncwarp();
     return;
@@ -568,16 +570,23 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   const int64_t r0 = range_of(S0), r1 = range_of(E0 - 1);
   if (r0 == r1) return;   // one segment: written by the decode kernel
   const bool first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
+  // ranges between r0 and r1 may be empty (fewer blocks than ranges): they
+  // wrote nothing for this (b, g) and are skipped
+  auto touches = [&](int64_t r) {
+    return range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
+  };
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, e = idx % D;
     float M = -INFINITY;
     for (int64_t r = r0; r <= r1; ++r) {
+      if (!touches(r)) continue;
       const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
       M = fmaxf(M, p.ws_ml[(sl * G + h) * 2]);
     }
     const float ref = (M == -INFINITY) ? 0.f : M;
     float L = 0.f, O = 0.f;
     for (int64_t r = r0; r <= r1; ++r) {
+      if (!touches(r)) continue;
       const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
       const float wgt = exp2f(p.ws_ml[(sl * G + h) * 2] - ref);
       L += wgt * p.ws_ml[(sl * G + h) * 2 + 1];

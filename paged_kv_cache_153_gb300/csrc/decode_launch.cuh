@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "decode.cuh"
+#include "host_util.h"
 
 namespace pkv {
 
@@ -31,28 +32,36 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   if (stages > 32) stages = 32;
   size_t smem = Tr::smem_bytes(stages, p.batch, p.n_kv_heads);
   int max_optin = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+  if (cuda_failed(cudaGetDevice(&dev), "cudaGetDevice")) return PKV_ERR_CUDA;
+  if (cuda_failed(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+                  "cudaDeviceGetAttribute"))
     return PKV_ERR_CUDA;
-  while (smem > static_cast<size_t>(max_optin) && stages > 2) {
+  cudaFuncAttributes fattr;
+  if (cuda_failed(cudaFuncGetAttributes(&fattr, kern), "cudaFuncGetAttributes")) return PKV_ERR_CUDA;
+  // dynamic shared memory may use what the static part leaves of the opt-in limit
+  const size_t dyn_max = static_cast<size_t>(max_optin) - fattr.sharedSizeBytes;
+  while (smem > dyn_max && stages > 2) {
     --stages;
     smem = Tr::smem_bytes(stages, p.batch, p.n_kv_heads);
   }
-  if (smem > static_cast<size_t>(max_optin)) return PKV_ERR_UNSUPPORTED;   // batch too large for one block
-  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  if (smem > dyn_max) return PKV_ERR_UNSUPPORTED;   // batch too large for one block's shared memory
+  // the opt-in is a per-device function attribute: set it once per device
   static std::mutex attr_mu;
   static bool attr_done[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
   {
     std::lock_guard<std::mutex> lock(attr_mu);
     if (!attr_done[dev]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) != cudaSuccess)
+      if (cuda_failed(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(dyn_max)),
+                      "cudaFuncSetAttribute"))
         return PKV_ERR_CUDA;
       attr_done[dev] = true;
     }
   }
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Tr::kThreads, smem) != cudaSuccess)
+  if (cuda_failed(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Tr::kThreads, smem),
+                  "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
   if (occ > li.max_ctas_per_sm) occ = li.max_ctas_per_sm;
@@ -63,11 +72,11 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   li.grid = grid;
   li.stages = stages;
   kern<<<grid, Tr::kThreads, smem, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  if (cuda_failed(cudaGetLastError(), "paged_decode_kernel launch")) return PKV_ERR_CUDA;
   const int units = p.batch * p.n_kv_heads;
   if (units > 0) {
     paged_decode_combine_kernel<QT, D, G><<<units, 128, 0, stream>>>(p, grid);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (cuda_failed(cudaGetLastError(), "paged_decode_combine_kernel launch")) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }

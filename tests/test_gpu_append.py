@@ -120,7 +120,7 @@ def test_fp8_append_special_values(pkv):
     # saturation boundary and signed zeros, with scale 1
     vals = oe.decode(np.arange(0x7F))
     mids = (vals[:-1] + vals[1:]) / 2
-    special = np.array([0.0, -0.0, 448.0, 449.0, 464.0, 480.0, 1e4, -1e4, 2.0 ** -10, 3 * 2.0 ** -10,
+    special = np.array([0.0, -0.0, 448.0, 450.0, 464.0, 480.0, 1024.0, -16384.0, 2.0 ** -10, 3 * 2.0 ** -10,
                         -2.0 ** -12])
     x = np.concatenate([vals, -vals, mids, -mids, special]).astype(np.float32)
     # bf16 holds every E4M3 value and midpoint exactly
