@@ -156,6 +156,40 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
                                       void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged decode attention without a workspace argument, for callers that
+ * cannot allocate device memory: a plugin or C host program whose host
+ * application owns every device allocation and exposes no allocator, or a
+ * latency-critical loop where cudaMalloc / cudaFree (which synchronise the
+ * device) are not allowed.  The pages have no counterpart: this is a calling
+ * convention, not part of the method.
+ *
+ * Computes exactly what pkv_paged_decode_attention computes (same arguments,
+ * minus workspace / workspace_bytes).  The scratch is one file-scope device
+ * array of PKV_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library
+ * holds until the process exits.  This function allocates nothing.
+ *   - Limit: a call whose pkv_decode_workspace_bytes(...) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES (16 MiB) is refused with PKV_ERR_WORKSPACE.
+ *     The balanced split (partition_tokens = 0) needs about 5 MB at most on a
+ *     152-SM GPU (head_dim 128, group 8) plus 4 bytes per sequence, so it
+ *     fits; a fixed partition split of many long contexts may not.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Sharing: every call on a device uses the same array and it keeps the
+ *     last call's contents; the kernel writes each scratch word before reading
+ *     it, so nothing needs clearing.  Calls that overlap on the GPU (other
+ *     streams, or other host threads) race on the scratch: serialise them.
+ * ------------------------------------------------------------------------- */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+pkv_status pkv_paged_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                              int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                              float scale, void* out, pkv_dtype dtype, int partition_tokens,
+                                              int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Paged decode attention over an E4M3 cache (uint8 codes) with per-KV-head
  * scales: K_j and V_j above are replaced by E4M3(code) * k_scale[g] and
  * E4M3(code) * v_scale[g], dequantised in registers before the arithmetic

@@ -20,6 +20,7 @@ __all__ = [
     "PKV_F16", "PKV_BF16", "PkvError", "lib", "library_path",
     "pkv_slot_mapping", "pkv_kv_append", "pkv_kv_append_fp8", "pkv_decode_workspace_bytes",
     "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8", "pkv_decode_step_host",
+    "pkv_paged_decode_attention_noalloc",
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
 ]
 
@@ -46,6 +47,8 @@ _SIGS = {
                                         _p, _sz, _p, _p]),
     "pkv_paged_decode_attention_fp8": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f,
                                             _p, _i, _i, _p, _sz, _p, _p]),
+    "pkv_paged_decode_attention_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
+                                                _i, _p, _p]),
     "pkv_decode_step_host": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i,
                                   _i, _i, _i64, _i, _f, _i, _i, _p, _sz, _p, _p]),
     "pkv_pool_create": (_p, [_i64, _i]),
@@ -168,6 +171,19 @@ def pkv_paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
         _ptr(context_lens), b, hq, hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale, _ptr(out),
         _dtype_code(q, q_dtype), partition_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, out, *, scale: float,
+                                       max_context_len: int, partition_tokens: int = 0, dtype=None,
+                                       err_flag=None, stream=None) -> None:
+    """Decode attention with the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate)."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_decode_attention_noalloc", lib.pkv_paged_decode_attention_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), b, hq, hkv, d, bs,
+        block_tables.shape[1], nb, max_context_len, scale, _ptr(out), _dtype_code(q, dtype), partition_tokens,
         _ptr(err_flag), _stream(stream)))
 
 
