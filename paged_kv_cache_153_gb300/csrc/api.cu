@@ -9,6 +9,8 @@
 #include "decode_launch.cuh"
 #include "host_util.h"
 
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <cstring>
 
@@ -23,6 +25,37 @@ bool cuda_failed(cudaError_t e, const char* what) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e),
                 cudaGetErrorString(e));
   cudaGetLastError();   // clear the non-sticky error state
+  return true;
+}
+
+bool encode_cache_tmap(CUtensorMap* map, const void* base, int64_t rows, int head_dim, int elt_bytes) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static cudaError_t lookup_err = cudaSuccess;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    lookup_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (lookup_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (encode == nullptr) {
+    cuda_failed(lookup_err == cudaSuccess ? cudaErrorSymbolNotFound : lookup_err,
+                "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+    return false;
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elt_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt_bytes), 16};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled: CUresult %d", static_cast<int>(r));
+    return false;
+  }
   return true;
 }
 

@@ -17,6 +17,7 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ tables, int max_
                                     const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ positions,
                                     int32_t offset, int64_t n_tokens, int64_t* __restrict__ slots,
                                     int32_t* err) {
+  pdl_wait_and_release();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n_tokens) return;
   const int64_t b = seq_idx ? seq_idx[t] : t;
@@ -45,6 +46,7 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
                                  const int64_t* __restrict__ slots, int64_t n_tokens, uint4* __restrict__ k_cache,
                                  uint4* __restrict__ v_cache, int64_t num_slots, int n_heads, int chunks_per_row,
                                  int32_t* err) {
+  pdl_wait_and_release();
   const int64_t per_kv = n_tokens * n_heads * chunks_per_row;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= 2 * per_kv) return;
@@ -82,6 +84,7 @@ __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint
                                      uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
                                      const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                                      int64_t num_slots, int n_heads, int chunks_per_row, int32_t* err) {
+  pdl_wait_and_release();
   const int64_t per_kv = n_tokens * n_heads * chunks_per_row;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= 2 * per_kv) return;
@@ -122,10 +125,6 @@ using namespace pkv;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static pkv_status launch_status(const char* what) {
-  return cuda_failed(cudaGetLastError(), what) ? PKV_ERR_CUDA : PKV_OK;
-}
-
 extern "C" pkv_status pkv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq, int64_t num_blocks,
                                        const int32_t* seq_idx, const int32_t* positions, int32_t position_offset,
                                        int64_t num_tokens, int block_size, int64_t* slot_mapping,
@@ -136,10 +135,11 @@ extern "C" pkv_status pkv_slot_mapping(const int32_t* block_tables, int max_bloc
   if (!block_tables || !positions || !slot_mapping) return PKV_ERR_INVALID_ARG;
   const int threads = 128;
   const int64_t grid = (num_tokens + threads - 1) / threads;
-  slot_mapping_kernel<<<static_cast<unsigned>(grid), threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      block_tables, max_blocks_per_seq, num_blocks, seq_idx, positions, position_offset, num_tokens,
-      slot_mapping, err_flag);
-  return launch_status("slot_mapping_kernel launch");
+  const cudaError_t e = launch_pdl(slot_mapping_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0,
+                                   static_cast<cudaStream_t>(stream), block_tables, max_blocks_per_seq,
+                                   num_blocks, seq_idx, positions, position_offset, num_tokens, slot_mapping,
+                                   err_flag);
+  return cuda_failed(e, "slot_mapping_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }
 
 extern "C" pkv_status pkv_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -157,11 +157,12 @@ extern "C" pkv_status pkv_kv_append(const void* k_new, const void* v_new, const 
   const int64_t total = 2 * num_tokens * num_kv_heads * chunks;
   const int threads = 256;
   const int64_t grid = (total + threads - 1) / threads;
-  kv_append_kernel<<<static_cast<unsigned>(grid), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+  const cudaError_t e = launch_pdl(
+      kv_append_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, static_cast<cudaStream_t>(stream),
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks * kBlockSize, num_kv_heads, chunks,
       err_flag);
-  return launch_status("kv_append_kernel launch");
+  return cuda_failed(e, "kv_append_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }
 
 extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -182,15 +183,10 @@ extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, co
   const int threads = 256;
   const unsigned grid = static_cast<unsigned>((total + threads - 1) / threads);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_dtype == PKV_F16)
-    kv_append_fp8_kernel<F16><<<grid, threads, 0, s>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
-        reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale, v_scale,
-        num_blocks * kBlockSize, num_kv_heads, chunks, err_flag);
-  else
-    kv_append_fp8_kernel<BF16><<<grid, threads, 0, s>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
-        reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale, v_scale,
-        num_blocks * kBlockSize, num_kv_heads, chunks, err_flag);
-  return launch_status("kv_append_fp8_kernel launch");
+  auto kern = (in_dtype == PKV_F16) ? kv_append_fp8_kernel<F16> : kv_append_fp8_kernel<BF16>;
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(threads), 0, s, static_cast<const uint4*>(k_new),
+                                   static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
+                                   reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale,
+                                   v_scale, num_blocks * kBlockSize, num_kv_heads, chunks, err_flag);
+  return cuda_failed(e, "kv_append_fp8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }

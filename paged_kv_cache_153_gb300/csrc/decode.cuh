@@ -19,22 +19,32 @@
 //
 // Thread block.  NW consumer warps + 1 producer warp.  The producer walks the
 // segments, reads block ids from the table (32 at a time, one per lane) and
-// issues one 1-D bulk copy (TMA) per K slab and per V slab -- each
-// [16, head_dim] slab of a (block, KV head) is contiguous in the
-// (num_blocks, H_kv, 16, head_dim) layout -- into a ring of `stages` shared
-// memory stages guarded by full/empty mbarriers.  The query rows of the next
-// segment travel the same way through a 2-deep ring together with the
-// segment's descriptor.  Consumer warp w takes every NW-th block of the range.
+// stages each (block, KV head) slab of K and of V -- [16, head_dim], contiguous
+// in the (num_blocks, H_kv, 16, head_dim) layout -- into shared memory with
+// TMA: one 1-D bulk copy per slab (linear layout), or, for the tensor-core
+// consumer, tiled tensor copies of [16 rows x 128 bytes] with the 128-byte
+// swizzle so that ldmatrix reads are free of bank conflicts.  The CTA's
+// blocks are dealt round-robin to the consumer warps (block k -> warp k % NW)
+// and every warp owns a private ring of S / NW stages, so a warp only ever
+// waits on a stage whose previous phase it consumed itself.  The query rows of
+// the next segment travel through a 2-deep ring with the segment descriptor.
 //
-// Consumer arithmetic (fp32).  A token row is split over LPT = D / 8 lanes
-// (8 elements, 16 bytes per lane); a warp covers 32 / LPT token rows at once.
-// Partial dot products for the G heads are reduced across the LPT lanes by a
-// butterfly reduce-scatter, the block maximum by shuffles, the probabilities
-// are shared through a per-warp scratch row, and p.V accumulates in registers
-// with each lane owning 8 output elements of every head.  Scores are kept in
-// the log2 domain (scale * log2(e) folded into q), so exponentials are exp2.
+// Consumers.  Scores are kept in the log2 domain (scale * log2(e) applied in
+// fp32), so exponentials are exp2.
+//  * CUDA-core consumer (G = 1, E4M3 cache): a token row is split over
+//    LPT = D / 8 lanes; partial dot products are reduced by a butterfly
+//    reduce-scatter; p is shared through a per-warp scratch row; p.V
+//    accumulates in fp32 registers, each lane owning 8 output elements.
+//  * Tensor-core consumer (G >= 2, 16-bit cache): q.K^T of a block is one
+//    mma.m16n8k16 per 16 head_dim elements with the 16 tokens as M and the G
+//    query heads (zero-padded to 8) as N; the fp32 scores of the C fragment
+//    go through the online softmax in registers; p is rounded to the cache's
+//    16-bit type, transposed in registers (movmatrix) into the B operand of
+//    p.V, which accumulates O^T[head_dim x heads] in fp32 with V^T read by
+//    ldmatrix.trans.  The normaliser l sums the same rounded p.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "pkv_common.cuh"
@@ -42,6 +52,8 @@
 namespace pkv {
 
 struct DecodeParams {
+  CUtensorMap tmap_k;            // tiled views of the caches (tensor-core variant only)
+  CUtensorMap tmap_v;
   const void* q;                 // [B, Hq, D] 16-bit
   const void* k_cache;           // [NB, Hkv, 16, D] KV element type
   const void* v_cache;
@@ -62,7 +74,7 @@ struct DecodeParams {
   int max_nblk;                  // ceil(max_context_len / 16)
   int part_blocks;               // 0 = balanced ranges
   int slot_capacity;             // number of partial slots in the workspace
-  int stages;
+  int stages;                    // multiple of the consumer warp count
   float qk_scale_log2;           // softmax scale * log2(e)
 };
 
@@ -70,7 +82,7 @@ struct SegDesc {
   int b, g, i0, i1;              // logical blocks [i0, i1) of (b, g)
   int n_tokens;                  // valid tokens of (b, g)
   int nblk;                      // blocks of (b, g)
-  int slot;                      // -1 = write out directly, else partial slot
+  int slot;                      // -1 = write out directly, -2 = dropped, else partial slot
   int end;                       // 1 = no more segments
 };
 
@@ -94,22 +106,24 @@ __device__ __forceinline__ int64_t range_start(int64_t r, int64_t W, int64_t R, 
   return part_blocks ? min(r * part_blocks, W) : (r * W) / R;
 }
 
-template <int D, int G, int NW, typename KV>
+template <int D, int G, int NW, typename KV, bool MMA>
 struct DecodeTraits {
   static constexpr int kEsz = KV::kBytes;
   static constexpr int kSlab = kBlockSize * D * kEsz;          // bytes of one (block, head) slab
   static constexpr int kStage = 2 * kSlab;                     // K + V
+  static constexpr int kSubTiles = (D * kEsz) / 128;           // swizzled [16 x 128 B] tiles per slab
+  static constexpr int kQBytes = G * D * 2;
+  static constexpr int kThreads = (NW + 1) * 32;
+  // CUDA-core consumer geometry
   static constexpr int kLPT = D / 8;                           // lanes per token row
   static constexpr int kNTG = 32 / kLPT;                       // token groups per warp
   static constexpr int kTPG = kBlockSize / kNTG;               // tokens per group per block
   static constexpr int kNV = kTPG * G;                         // partial scores per lane
   static constexpr int kNF = (kNV >= kLPT) ? kNV / kLPT : 1;   // held scores after reduce-scatter
-  static constexpr int kQBytes = G * D * 2;
-  static constexpr int kThreads = (NW + 1) * 32;
   static_assert(kNF == (G >= 2 ? G / 2 : 1), "lane/head mapping");
+  static_assert(!MMA || (G >= 2 && G <= 8 && kEsz == 2 && (D * kEsz) % 128 == 0), "tensor-core variant");
 
-  // shared memory layout (byte offsets); the ring comes first (128-B aligned)
-  static __host__ __device__ size_t ring_off() { return 0; }
+  // shared memory layout (byte offsets from a 1024-byte aligned base)
   static __host__ __device__ size_t q_off(int stages) { return static_cast<size_t>(stages) * kStage; }
   static __host__ __device__ size_t p_off(int stages) { return q_off(stages) + 2 * kQBytes; }
   static __host__ __device__ size_t merge_off(int stages) {
@@ -119,16 +133,22 @@ struct DecodeTraits {
     return merge_off(stages) + sizeof(float) * NW * G * (D + 2);
   }
   static __host__ __device__ size_t misc_off(int stages) { return bar_off(stages) + 8 * (2 * stages + 4); }
-  static __host__ __device__ size_t cum_off(int stages, int n_kv_heads) {
-    // stage_ok[stages], seg[2], abort, scales[2 * Hkv]
-    size_t o = misc_off(stages) + 4 * stages + sizeof(SegDesc) * 2 + 16 + 4 * 2 * n_kv_heads;
-    return (o + 15) & ~static_cast<size_t>(15);
+  // misc: stage_ok[stages], seg[2], abort (16 B), warp totals (32 ints), scales[2 * Hkv]
+  static __host__ __device__ size_t scales_off(int stages) {
+    return misc_off(stages) + 4 * stages + sizeof(SegDesc) * 2 + 16 + 4 * 32;
   }
+  static __host__ __device__ size_t cum_off(int stages, int n_kv_heads) {
+    return (scales_off(stages) + 4 * 2 * n_kv_heads + 15) & ~static_cast<size_t>(15);
+  }
+  // + 1024 bytes so that the base can be rounded up to a 1024-byte boundary
   static __host__ __device__ size_t smem_bytes(int stages, int batch, int n_kv_heads) {
-    return cum_off(stages, n_kv_heads) + 4 * (2 * static_cast<size_t>(batch) + 2);
+    return 1024 + cum_off(stages, n_kv_heads) + 4 * (2 * static_cast<size_t>(batch) + 2);
   }
 };
 
+// ---------------------------------------------------------------------------
+// warp-level helpers
+// ---------------------------------------------------------------------------
 // butterfly reduce-scatter step over lanes xor MASK on N values
 template <int N, int MASK>
 __device__ __forceinline__ void rs_step(float* v, int lane) {
@@ -154,13 +174,75 @@ __device__ __forceinline__ void reduce_scatter(float* v, int lane) {
   }
 }
 
-template <typename QT, typename KV, int D, int G, int NW>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const DecodeParams p) {
-  using T = DecodeTraits<D, G, NW, KV>;
-  constexpr int LPT = T::kLPT, TPG = T::kTPG, NF = T::kNF;
-  extern __shared__ __align__(128) unsigned char smem[];
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1, BF16) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1, F16) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// two floats -> packed 16-bit pair (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, BF16) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, F16) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2-D tiled TMA load of a [16 x 128 B] box at (x elements, y rows)
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// address of 16-byte chunk `chunk` of row `row` in a slab staged as 128B-swizzled
+// [16 x 128 B] sub-tiles (each 2 KiB, 1024-byte aligned)
+__device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int row, int chunk) {
+  return slab + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// the decode kernel
+// ---------------------------------------------------------------------------
+template <typename QT, typename KV, int D, int G, int NW, bool MMA>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using T = DecodeTraits<D, G, NW, KV, MMA>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);   // 1024-byte aligned base
   const int S = p.stages;
-  unsigned char* ring = smem + T::ring_off();
+  const int SPW = S / NW;                                         // private stages per consumer warp
+  unsigned char* ring = smem;
   unsigned char* q_ring = smem + T::q_off(S);
   float* p_scr = reinterpret_cast<float*>(smem + T::p_off(S));
   float* merge = reinterpret_cast<float*>(smem + T::merge_off(S));
@@ -171,12 +253,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
   int* stage_ok = reinterpret_cast<int*>(smem + T::misc_off(S));
   SegDesc* seg = reinterpret_cast<SegDesc*>(smem + T::misc_off(S) + 4 * S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc));
-  float* scales = reinterpret_cast<float*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc) + 16);
+  int* warp_tot = reinterpret_cast<int*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc) + 16);
+  float* scales = reinterpret_cast<float*>(smem + T::scales_off(S));
   int* cum = reinterpret_cast<int*>(smem + T::cum_off(S, p.n_kv_heads));   // [B + 1]
   int* ntok = cum + p.batch + 1;                                             // [B]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads;
+  pdl_wait_and_release();
 
   // ---- 1. per-sequence block counts and their prefix (all threads) -------
   if (tid == 0) *abort_flag = 0;
@@ -193,26 +277,24 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       nb = seq_blocks(p, ctx, p.err);
       ntok[b] = min(max(ctx, 0), nb * kBlockSize);
     }
-    // inclusive block-wide scan of nb
-    int x = nb;
+    int x = nb;   // inclusive block-wide scan
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    __shared__ int warp_tot[32];
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     int before = 0;
     for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
     if (b < p.batch) cum[b + 1] = carry + before + x;
     int tot = 0;
-    for (int w2 = 0; w2 < (int)(blockDim.x >> 5); ++w2) tot += warp_tot[w2];
+    for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) tot += warp_tot[w2];
     carry += tot;
     __syncthreads();
   }
-  if (tid == 0) cum[0] = 0;
   if (tid == 0) {
+    cum[0] = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -236,6 +318,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
     const char* qbase = static_cast<const char*>(p.q);
+    if (MMA && lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
+    }
     uint32_t k = 0, j = 0;
     for (int64_t r = blockIdx.x; r < R && !*abort_flag; r += (p.part_blocks ? gridDim.x : R)) {
       const int64_t f_lo = range_start(r, W, R, p.part_blocks);
@@ -293,19 +379,28 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
           for (int jj = 0; jj < cnt; ++jj) {
             const int pid = __shfl_sync(0xffffffffu, ids, jj);
             if (lane == 0) {
-              const int s = k % S;
-              if (k >= static_cast<uint32_t>(S) && !*abort_flag &&
-                  !mbar_wait(&empty_bar[s], ((k / S) - 1) & 1, p.err))
-                *abort_flag = 1;
+              const uint32_t jw = k / NW;                       // this block's index in its warp's ring
+              const int s = static_cast<int>(k % NW) + NW * static_cast<int>(jw % SPW);
+              const uint32_t use = jw / SPW;
+              if (use >= 1 && !*abort_flag && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.err)) *abort_flag = 1;
               const bool ok = pid >= 0 && pid < p.num_blocks && !*abort_flag;
               stage_ok[s] = ok ? 1 : 0;
+              unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
               if (ok) {
-                const int64_t slab = (static_cast<int64_t>(pid) * Hkv + g) * T::kSlab;
                 mbar_arrive_expect_tx(&full_bar[s], T::kStage);
-                bulk_g2s(ring + static_cast<size_t>(s) * T::kStage, kbase + slab, T::kSlab, &full_bar[s],
-                         pol_stream);
-                bulk_g2s(ring + static_cast<size_t>(s) * T::kStage + T::kSlab, vbase + slab, T::kSlab,
-                         &full_bar[s], pol_stream);
+                if constexpr (MMA) {
+                  const int y = (pid * Hkv + g) * kBlockSize;
+#pragma unroll
+                  for (int t = 0; t < T::kSubTiles; ++t) {
+                    tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
+                    tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
+                                pol_stream);
+                  }
+                } else {
+                  const int64_t slab = (static_cast<int64_t>(pid) * Hkv + g) * T::kSlab;
+                  bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
+                  bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
+                }
               } else {
                 if (!*abort_flag) record_error(p.err, PKV_ERR_OOB);
                 mbar_arrive(&full_bar[s]);
@@ -327,10 +422,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       mbar_arrive(&qfull_bar[qs]);
       // Before exiting, make sure no copy issued by this warp is still in
       // flight into shared memory (one overall time limit for the drain).
+      // The last S blocks occupy S distinct stages.
       const unsigned long long deadline = global_ns() + kWaitLimitNs;
       const uint32_t first = k > static_cast<uint32_t>(S) ? k - S : 0;
-      for (uint32_t kk = first; kk < k; ++kk)
-        if (stage_ok[kk % S]) mbar_wait_until(&full_bar[kk % S], (kk / S) & 1, deadline);
+      for (uint32_t kk = first; kk < k; ++kk) {
+        const uint32_t jw = kk / NW;
+        const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
+        if (stage_ok[s]) mbar_wait_until(&full_bar[s], (jw / SPW) & 1, deadline);
+      }
       // Only the last segment's query copy can still be in flight: the one
       // before it shares its slot with the end marker, whose publication
       // waited until the consumers had read that copy (and re-armed the slot).
@@ -341,13 +440,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
   }
 
   // ========================== consumer warps ===============================
-  const int li = lane & (LPT - 1);       // owns elements [8 li, 8 li + 8) of a row
-  const int tg = lane / LPT;             // token group
-  const int hsel = lane & 1;             // which half of the heads this lane holds
+  constexpr int LPT = T::kLPT, TPG = T::kTPG, NF = T::kNF;
+  const int li = lane & (LPT - 1);       // CUDA-core: owns elements [8 li, 8 li + 8) of a row
+  const int tg = lane / LPT;             // CUDA-core: token group
+  const int hsel = lane & 1;             // CUDA-core: which half of the heads this lane holds
   const int t_held = tg * TPG + (li >> 1);
   float* pw = p_scr + warp * kBlockSize * G;
+  // tensor-core lane geometry (C fragment: tokens lane/4 and lane/4 + 8, heads 2 (lane%4) + {0, 1})
+  const int q4 = lane & 3, r4 = lane >> 2;
+  const int h0 = 2 * q4;
+  const int mrow = lane & 7, mi = lane >> 3;      // ldmatrix: row within matrix, matrix index
   uint32_t j = 0;
-  uint32_t k_base = 0;                   // flat counter of the segment's first block in this CTA
+  uint32_t k_base = 0;                   // CTA-local counter of the segment's first block
   while (true) {
     const int qs = j & 1;
     const bool got = !*abort_flag && mbar_wait(&qfull_bar[qs], (j >> 1) & 1, p.err);
@@ -355,159 +459,260 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
     // every consumer warp must take the same exit decision (named barriers follow)
     if (named_bar_red_or(2, NW * 32, !got || seg[qs].end)) break;
     const SegDesc d = seg[qs];
-    float qf[G][8];
-    {
-      const float qscale = p.qk_scale_log2 * scales[d.g];
-      const unsigned char* qrow = q_ring + qs * T::kQBytes;
+    const unsigned char* qrow = q_ring + qs * T::kQBytes;
+    const float sc = p.qk_scale_log2 * scales[d.g];
+    const int nseg = d.i1 - d.i0;
+    const int first = static_cast<int>((warp + NW - (k_base % NW)) % NW);   // first local index for this warp
+    float* mw = merge + warp * G * (D + 2);        // [G][D] o, then [G] m, [G] l
+
+    if constexpr (MMA) {
+      // ------------------------- tensor-core consumer -------------------------
+      constexpr int KS = D / 16;
+      uint32_t bq[KS][2];
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const bool live = r4 < G;
+        const unsigned char* qh = qrow + ((live ? r4 : 0) * D + 16 * ks + 2 * q4) * 2;
+        bq[ks][0] = live ? *reinterpret_cast<const uint32_t*>(qh) : 0u;
+        bq[ks][1] = live ? *reinterpret_cast<const uint32_t*>(qh + 16) : 0u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty_bar[qs]);
+      float o[KS][4];
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      const int krow = mrow + 8 * (mi & 1), kchunk = mi >> 1;   // A of q.K^T
+      const int vrow = mrow + 8 * (mi >> 1), vchunk = mi & 1;   // A of p.V (transposed load)
+      for (int ii = first; ii < nseg; ii += NW) {
+        const uint32_t kk = k_base + ii;
+        const uint32_t jw = kk / NW;
+        const int s = warp + NW * static_cast<int>(jw % SPW);
+        if (*abort_flag || !mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int i = d.i0 + ii;
+        const int n_valid = stage_ok[s] ? min(kBlockSize, d.n_tokens - i * kBlockSize) : 0;
+        const uint32_t kslab = smem_u32(ring + static_cast<size_t>(s) * T::kStage);
+        const uint32_t vslab = kslab + T::kSlab;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(swz_addr(kslab, krow, 2 * ks + kchunk), a);
+          mma16816(c, a, bq[ks][0], bq[ks][1], QT{});
+        }
+        const bool v0 = r4 < n_valid, v1 = r4 + 8 < n_valid;
+        const float s00 = v0 ? c[0] * sc : -INFINITY, s01 = v0 ? c[1] * sc : -INFINITY;
+        const float s10 = v1 ? c[2] * sc : -INFINITY, s11 = v1 ? c[3] * sc : -INFINITY;
+        float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, msk));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, msk));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0, ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+        const uint32_t x0 = pack2(exp2f(s00 - ref0), exp2f(s01 - ref1), QT{});   // tokens 0..7
+        const uint32_t x1 = pack2(exp2f(s10 - ref0), exp2f(s11 - ref1), QT{});   // tokens 8..15
+        const float2 p0 = unpack2(x0, QT{}), p1 = unpack2(x1, QT{});
+        l0 = l0 * a0 + (p0.x + p1.x);
+        l1 = l1 * a1 + (p0.y + p1.y);
+        const bool resc = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
+        m0 = mn0;
+        m1 = mn1;
+        const uint32_t b0 = movmatrix_trans(x0), b1 = movmatrix_trans(x1);
+        if (resc) {
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_trans(swz_addr(vslab, vrow, 2 * mt + vchunk), a);
+          mma16816(o[mt], a, b0, b1, QT{});
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      k_base += nseg;
+      // sum l over the lanes of a head column; write o, m, l to the merge area
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
+      }
+      if (h0 < G) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          mw[h0 * D + 16 * mt + r4] = o[mt][0];
+          mw[(h0 + 1) * D + 16 * mt + r4] = o[mt][1];
+          mw[h0 * D + 16 * mt + r4 + 8] = o[mt][2];
+          mw[(h0 + 1) * D + 16 * mt + r4 + 8] = o[mt][3];
+        }
+        if (r4 == 0) {
+          mw[G * D + h0] = m0;
+          mw[G * D + h0 + 1] = m1;
+          mw[G * D + G + h0] = l0;
+          mw[G * D + G + h0 + 1] = l1;
+        }
+      }
+    } else {
+      // -------------------------- CUDA-core consumer --------------------------
+      float qf[G][8];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         load8(qrow + (h * D + li * 8) * 2, qf[h], QT{});
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qf[h][e] *= qscale;
+        for (int e = 0; e < 8; ++e) qf[h][e] *= sc;
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&qempty_bar[qs]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty_bar[qs]);
 
-    float m_run[G], l_part[NF], acc[G][8];
+      float m_run[G], l_part[NF], acc[G][8];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m_run[h] = -INFINITY;
+      for (int h = 0; h < G; ++h) {
+        m_run[h] = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-    }
-#pragma unroll
-    for (int x = 0; x < NF; ++x) l_part[x] = 0.f;
-
-    const int nseg = d.i1 - d.i0;
-    int first = static_cast<int>((warp + NW - (k_base % NW)) % NW);   // first local index for this warp
-    for (int ii = first; ii < nseg; ii += NW) {
-      const uint32_t k = k_base + ii;
-      const int s = k % S;
-      if (*abort_flag || !mbar_wait(&full_bar[s], (k / S) & 1, p.err)) {
-        *abort_flag = 1;
-        break;
+        for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
       }
-      const int i = d.i0 + ii;
-      const int n_valid = stage_ok[s] ? min(kBlockSize, d.n_tokens - i * kBlockSize) : 0;
-      const unsigned char* kslab = ring + static_cast<size_t>(s) * T::kStage;
-      const unsigned char* vslab = kslab + T::kSlab;
-
-      // ---- scores: partial dot products over this lane's 8 elements ----
-      float part[T::kNV];
 #pragma unroll
-      for (int i2 = 0; i2 < TPG; ++i2) {
-        float kf[8];
-        load8(kslab + ((tg * TPG + i2) * D + li * 8) * T::kEsz, kf, KV{});
+      for (int x = 0; x < NF; ++x) l_part[x] = 0.f;
+
+      for (int ii = first; ii < nseg; ii += NW) {
+        const uint32_t kk = k_base + ii;
+        const uint32_t jw = kk / NW;
+        const int s = warp + NW * static_cast<int>(jw % SPW);
+        if (*abort_flag || !mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int i = d.i0 + ii;
+        const int n_valid = stage_ok[s] ? min(kBlockSize, d.n_tokens - i * kBlockSize) : 0;
+        const unsigned char* kslab = ring + static_cast<size_t>(s) * T::kStage;
+        const unsigned char* vslab = kslab + T::kSlab;
+
+        // ---- scores: partial dot products over this lane's 8 elements ----
+        float part[T::kNV];
+#pragma unroll
+        for (int i2 = 0; i2 < TPG; ++i2) {
+          float kf[8];
+          load8(kslab + ((tg * TPG + i2) * D + li * 8) * T::kEsz, kf, KV{});
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float a0 = qf[h][0] * kf[0], a1 = qf[h][1] * kf[1];
+#pragma unroll
+            for (int e = 2; e < 8; e += 2) {
+              a0 = fmaf(qf[h][e], kf[e], a0);
+              a1 = fmaf(qf[h][e + 1], kf[e + 1], a1);
+            }
+            part[i2 * G + h] = a0 + a1;
+          }
+        }
+        reduce_scatter<T::kNV, LPT / 2>(part, lane);
+
+        // ---- online softmax over the block --------------------------------
+        float scv[NF], bm[NF];
+#pragma unroll
+        for (int x = 0; x < NF; ++x) {
+          scv[x] = (t_held < n_valid) ? part[x] : -INFINITY;
+          bm[x] = scv[x];
+        }
+#pragma unroll
+        for (int msk = 2; msk < 32; msk <<= 1)
+#pragma unroll
+          for (int x = 0; x < NF; ++x) bm[x] = fmaxf(bm[x], __shfl_xor_sync(0xffffffffu, bm[x], msk));
+        float bmax[G];
+        if constexpr (G == 1) {
+          bmax[0] = bm[0];
+        } else {
+#pragma unroll
+          for (int x = 0; x < NF; ++x) {
+            const float other = __shfl_xor_sync(0xffffffffu, bm[x], 1);
+            bmax[x] = hsel ? other : bm[x];
+            bmax[NF + x] = hsel ? bm[x] : other;
+          }
+        }
+        float m_new[G], alpha[G];
+        bool rescale = false;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float a0 = qf[h][0] * kf[0], a1 = qf[h][1] * kf[1];
-#pragma unroll
-          for (int e = 2; e < 8; e += 2) {
-            a0 = fmaf(qf[h][e], kf[e], a0);
-            a1 = fmaf(qf[h][e + 1], kf[e + 1], a1);
-          }
-          part[i2 * G + h] = a0 + a1;
+          m_new[h] = fmaxf(m_run[h], bmax[h]);
+          const float ref = (m_new[h] == -INFINITY) ? 0.f : m_new[h];
+          alpha[h] = exp2f(m_run[h] - ref);
+          rescale |= (m_new[h] != m_run[h]);
+          m_run[h] = m_new[h];
         }
-      }
-      reduce_scatter<T::kNV, LPT / 2>(part, lane);
-
-      // ---- online softmax over the block --------------------------------
-      float sc[NF], bm[NF];
 #pragma unroll
-      for (int x = 0; x < NF; ++x) {
-        sc[x] = (t_held < n_valid) ? part[x] : -INFINITY;
-        bm[x] = sc[x];
+        for (int x = 0; x < NF; ++x) {
+          const int h = (G == 1) ? 0 : (hsel ? NF + x : x);
+          float mh = m_new[0], ah = alpha[0];
+#pragma unroll
+          for (int hh = 1; hh < G; ++hh)
+            if (hh == h) { mh = m_new[hh]; ah = alpha[hh]; }
+          const float ref = (mh == -INFINITY) ? 0.f : mh;
+          const float pr = exp2f(scv[x] - ref);
+          l_part[x] = l_part[x] * ah + pr;
+          pw[t_held * G + h] = pr;
+        }
+        __syncwarp();
+        if (rescale) {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[h][e] *= alpha[h];
+        }
+        // ---- p . V --------------------------------------------------------
+#pragma unroll
+        for (int i2 = 0; i2 < TPG; ++i2) {
+          const int t = tg * TPG + i2;
+          float vf[8];
+          load8(vslab + (t * D + li * 8) * T::kEsz, vf, KV{});
+          float pv[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) pv[h] = pw[t * G + h];
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pv[h], vf[e], acc[h][e]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
+      k_base += nseg;
+
+      // ---- merge the warp's state ------------------------------------------
+#pragma unroll
+      for (int msk = LPT; msk < 32; msk <<= 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], msk);
 #pragma unroll
       for (int msk = 2; msk < 32; msk <<= 1)
 #pragma unroll
-        for (int x = 0; x < NF; ++x) bm[x] = fmaxf(bm[x], __shfl_xor_sync(0xffffffffu, bm[x], msk));
-      float bmax[G];
-      if constexpr (G == 1) {
-        bmax[0] = bm[0];
-      } else {
-#pragma unroll
-        for (int x = 0; x < NF; ++x) {
-          const float other = __shfl_xor_sync(0xffffffffu, bm[x], 1);
-          bmax[x] = hsel ? other : bm[x];
-          bmax[NF + x] = hsel ? bm[x] : other;
-        }
-      }
-      float m_new[G], alpha[G];
-      bool rescale = false;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m_new[h] = fmaxf(m_run[h], bmax[h]);
-        const float ref = (m_new[h] == -INFINITY) ? 0.f : m_new[h];
-        alpha[h] = exp2f(m_run[h] - ref);
-        rescale |= (m_new[h] != m_run[h]);
-        m_run[h] = m_new[h];
-      }
-#pragma unroll
-      for (int x = 0; x < NF; ++x) {
-        const int h = (G == 1) ? 0 : (hsel ? NF + x : x);
-        float mh = m_new[0], ah = alpha[0];
-#pragma unroll
-        for (int hh = 1; hh < G; ++hh)
-          if (hh == h) { mh = m_new[hh]; ah = alpha[hh]; }
-        const float ref = (mh == -INFINITY) ? 0.f : mh;
-        const float pr = exp2f(sc[x] - ref);
-        l_part[x] = l_part[x] * ah + pr;
-        pw[t_held * G + h] = pr;
-      }
-      __syncwarp();
-      if (rescale) {
+        for (int x = 0; x < NF; ++x) l_part[x] += __shfl_xor_sync(0xffffffffu, l_part[x], msk);
+      if (lane < LPT) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] *= alpha[h];
+          for (int e = 0; e < 8; ++e) mw[h * D + li * 8 + e] = acc[h][e];
       }
-      // ---- p . V --------------------------------------------------------
+      if (lane == 0) {
 #pragma unroll
-      for (int i2 = 0; i2 < TPG; ++i2) {
-        const int t = tg * TPG + i2;
-        float vf[8];
-        load8(vslab + (t * D + li * 8) * T::kEsz, vf, KV{});
-        float pv[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) pv[h] = pw[t * G + h];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pv[h], vf[e], acc[h][e]);
+        for (int h = 0; h < G; ++h) mw[G * D + h] = m_run[h];
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      if (lane < 2) {
+#pragma unroll
+        for (int x = 0; x < NF; ++x) mw[G * D + G + ((G == 1) ? 0 : (hsel ? NF + x : x))] = l_part[x];
+      }
     }
-    k_base += nseg;
 
-    // ---- merge the warp's state, then the NW warps' states ---------------
-#pragma unroll
-    for (int msk = LPT; msk < 32; msk <<= 1)
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], msk);
-#pragma unroll
-    for (int msk = 2; msk < 32; msk <<= 1)
-#pragma unroll
-      for (int x = 0; x < NF; ++x) l_part[x] += __shfl_xor_sync(0xffffffffu, l_part[x], msk);
-    float* mw = merge + warp * G * (D + 2);        // [G][D] o, then [G] m, [G] l
-    if (lane < LPT) {
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mw[h * D + li * 8 + e] = acc[h][e];
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) mw[G * D + h] = m_run[h];
-    }
-    if (lane < 2) {
-#pragma unroll
-      for (int x = 0; x < NF; ++x) mw[G * D + G + ((G == 1) ? 0 : (hsel ? NF + x : x))] = l_part[x];
-    }
+    // ---- merge the NW warps' states and write the result ---------------------
     named_bar_sync(1, NW * 32);
     const float vscale = scales[Hkv + d.g];
     for (int idx = tid; idx < G * D; idx += NW * 32) {
@@ -545,18 +750,32 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
 // ---------------------------------------------------------------------------
 // combine: out[b, g*G + h] = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r over
 // the partial slots of (b, g); zeros for an empty context.  One thread block
-// per (b, g); (b, g) pairs written directly by the decode kernel are skipped.
+// per (b, g), one thread per 4 consecutive outputs, one online pass over the
+// partials; (b, g) pairs written directly by the decode kernel are skipped.
 // ---------------------------------------------------------------------------
+template <int D, int G>
+constexpr int combine_threads() {
+  return (G * D / 4) < 32 ? 32 : (G * D / 4);
+}
+
 template <typename QT, int D, int G>
-__global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p, int grid_ranges) {
+__global__ void __launch_bounds__(combine_threads<D, G>())
+    paged_decode_combine_kernel(const __grid_constant__ DecodeParams p, int grid_ranges) {
+  pdl_wait_and_release();
   const int u = blockIdx.x;
   const int b = u / p.n_kv_heads, g = u % p.n_kv_heads;
+  const int t = threadIdx.x;
+  if (t >= G * D / 4) return;
   auto* out = static_cast<typename QT::storage*>(p.out);
   const int c0 = p.ws_cum[b], c1 = p.ws_cum[b + 1];
   const int nb = c1 - c0;
-  const int64_t base_out = (static_cast<int64_t>(b) * p.n_q_heads + g * G) * D;
+  const int64_t base_out = (static_cast<int64_t>(b) * p.n_q_heads + g * G) * D + 4 * t;
+  auto store4 = [&](float a, float b2, float c, float d) {
+    const uint32_t lo = pack2(a, b2, QT{}), hi = pack2(c, d, QT{});
+    *reinterpret_cast<uint2*>(out + base_out) = make_uint2(lo, hi);
+  };
   if (nb == 0) {
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) out[base_out + idx] = to_out(0.f, QT{});
+    store4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int64_t W = static_cast<int64_t>(p.n_kv_heads) * p.ws_cum[p.batch];
@@ -570,30 +789,27 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   const int64_t r0 = range_of(S0), r1 = range_of(E0 - 1);
   if (r0 == r1) return;   // one segment: written by the decode kernel
   const bool first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
-  // ranges between r0 and r1 may be empty (fewer blocks than ranges): they
-  // wrote nothing for this (b, g) and are skipped
-  auto touches = [&](int64_t r) {
-    return range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
-  };
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int h = idx / D, e = idx % D;
-    float M = -INFINITY;
-    for (int64_t r = r0; r <= r1; ++r) {
-      if (!touches(r)) continue;
-      const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
-      M = fmaxf(M, p.ws_ml[(sl * G + h) * 2]);
-    }
-    const float ref = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, O = 0.f;
-    for (int64_t r = r0; r <= r1; ++r) {
-      if (!touches(r)) continue;
-      const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
-      const float wgt = exp2f(p.ws_ml[(sl * G + h) * 2] - ref);
-      L += wgt * p.ws_ml[(sl * G + h) * 2 + 1];
-      O += wgt * p.ws_o[(sl * G + h) * D + e];
-    }
-    out[base_out + idx] = to_out(L > 0.f ? O / L : 0.f, QT{});
+  const int h = (4 * t) / D, e = (4 * t) % D;
+  float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
+  for (int64_t r = r0; r <= r1; ++r) {
+    // ranges between r0 and r1 may be empty (fewer blocks than ranges): they
+    // wrote nothing for this (b, g) and are skipped
+    if (range_start(r + 1, W, R, p.part_blocks) <= range_start(r, W, R, p.part_blocks)) continue;
+    const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
+    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2);
+    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e);
+    const float mn = fmaxf(M, ml.x);
+    const float ref = (mn == -INFINITY) ? 0.f : mn;
+    const float a = exp2f(M - ref), w = exp2f(ml.x - ref);
+    L = L * a + w * ml.y;
+    O0 = O0 * a + w * o.x;
+    O1 = O1 * a + w * o.y;
+    O2 = O2 * a + w * o.z;
+    O3 = O3 * a + w * o.w;
+    M = mn;
   }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  store4(O0 * inv, O1 * inv, O2 * inv, O3 * inv);
 }
 
 }  // namespace pkv

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "decode.cuh"
@@ -13,24 +14,22 @@ namespace pkv {
 struct LaunchInfo {
   int num_sms;
   int max_ctas_per_sm;     // cap on resident decode blocks per SM
-  int stages;              // 0 = default for the variant
+  int stages;              // 0 = fill the SM's shared memory; else a request (rounded to the warp count)
   int grid;                // out: decode grid used
   int64_t part_ranges_cap; // partition mode: max ranges the workspace holds
 };
 
 using DecodeLauncher = pkv_status (*)(DecodeParams&, LaunchInfo&, cudaStream_t);
 
-constexpr int kDefaultRingBytes = 64 * 1024;
 constexpr int kMaxDevices = 64;
+constexpr int kSmemPerSm = 233472;        // shared memory per SM on sm_100-class parts (228 KiB)
+constexpr int kSmemReservedPerCta = 1024; // system-reserved shared memory per resident block
+constexpr int kMaxStagesPerWarp = 8;
 
-template <typename QT, typename KV, int D, int G, int NW>
+template <typename QT, typename KV, int D, int G, int NW, bool MMA>
 pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t stream) {
-  using Tr = DecodeTraits<D, G, NW, KV>;
-  auto kern = paged_decode_kernel<QT, KV, D, G, NW>;
-  int stages = li.stages > 0 ? li.stages : kDefaultRingBytes / Tr::kStage;
-  if (stages < 2) stages = 2;
-  if (stages > 32) stages = 32;
-  size_t smem = Tr::smem_bytes(stages, p.batch, p.n_kv_heads);
+  using Tr = DecodeTraits<D, G, NW, KV, MMA>;
+  auto kern = paged_decode_kernel<QT, KV, D, G, NW, MMA>;
   int max_optin = 0, dev = 0;
   if (cuda_failed(cudaGetDevice(&dev), "cudaGetDevice")) return PKV_ERR_CUDA;
   if (cuda_failed(cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
@@ -40,11 +39,6 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   if (cuda_failed(cudaFuncGetAttributes(&fattr, kern), "cudaFuncGetAttributes")) return PKV_ERR_CUDA;
   // dynamic shared memory may use what the static part leaves of the opt-in limit
   const size_t dyn_max = static_cast<size_t>(max_optin) - fattr.sharedSizeBytes;
-  while (smem > dyn_max && stages > 2) {
-    --stages;
-    smem = Tr::smem_bytes(stages, p.batch, p.n_kv_heads);
-  }
-  if (smem > dyn_max) return PKV_ERR_UNSUPPORTED;   // batch too large for one block's shared memory
   // the opt-in is a per-device function attribute: set it once per device
   static std::mutex attr_mu;
   static bool attr_done[kMaxDevices] = {};
@@ -59,24 +53,59 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
       attr_done[dev] = true;
     }
   }
+  // Stages come in multiples of NW (each consumer warp owns stages/NW of them).
+  // By default, the ring fills the SM's shared memory across as many resident
+  // blocks as the registers allow (capped by max_ctas_per_sm).
   int occ = 0;
+  size_t smem = Tr::smem_bytes(NW, p.batch, p.n_kv_heads);
+  if (smem > dyn_max) return PKV_ERR_UNSUPPORTED;   // batch too large for one block's shared memory
   if (cuda_failed(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Tr::kThreads, smem),
                   "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  if (occ > li.max_ctas_per_sm) occ = li.max_ctas_per_sm;
+  occ = std::min(occ, li.max_ctas_per_sm);
+  int spw = 1;
+  if (li.stages > 0) {
+    spw = std::max(1, li.stages / NW);
+  } else {
+    for (int cand = kMaxStagesPerWarp; cand >= 1; --cand) {
+      const size_t s = Tr::smem_bytes(NW * cand, p.batch, p.n_kv_heads);
+      if (s <= dyn_max && static_cast<size_t>(occ) * (s + kSmemReservedPerCta) <= kSmemPerSm) {
+        spw = cand;
+        break;
+      }
+    }
+  }
+  spw = std::min(spw, kMaxStagesPerWarp);
+  while (spw > 1 && Tr::smem_bytes(NW * spw, p.batch, p.n_kv_heads) > dyn_max) --spw;
+  const int stages = NW * spw;
+  smem = Tr::smem_bytes(stages, p.batch, p.n_kv_heads);
+  if (cuda_failed(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Tr::kThreads, smem),
+                  "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
+    return PKV_ERR_CUDA;
+  if (occ < 1) return PKV_ERR_UNSUPPORTED;
+  occ = std::min(occ, li.max_ctas_per_sm);
   int grid = li.num_sms * occ;
   if (p.part_blocks > 0 && li.part_ranges_cap < grid) grid = static_cast<int>(li.part_ranges_cap);
   if (grid < 1) grid = 1;
   p.stages = stages;
   li.grid = grid;
   li.stages = stages;
-  kern<<<grid, Tr::kThreads, smem, stream>>>(p);
-  if (cuda_failed(cudaGetLastError(), "paged_decode_kernel launch")) return PKV_ERR_CUDA;
+  if constexpr (MMA) {
+    const int64_t rows = p.num_blocks * p.n_kv_heads * kBlockSize;
+    if (rows > INT32_MAX) return PKV_ERR_UNSUPPORTED;    // TMA row coordinates are 32-bit
+    if (!encode_cache_tmap(&p.tmap_k, p.k_cache, rows, D, Tr::kEsz) ||
+        !encode_cache_tmap(&p.tmap_v, p.v_cache, rows, D, Tr::kEsz))
+      return PKV_ERR_CUDA;
+  }
+  if (cuda_failed(launch_pdl(kern, dim3(grid), dim3(Tr::kThreads), smem, stream, p), "paged_decode_kernel launch"))
+    return PKV_ERR_CUDA;
   const int units = p.batch * p.n_kv_heads;
   if (units > 0) {
-    paged_decode_combine_kernel<QT, D, G><<<units, 128, 0, stream>>>(p, grid);
-    if (cuda_failed(cudaGetLastError(), "paged_decode_combine_kernel launch")) return PKV_ERR_CUDA;
+    if (cuda_failed(launch_pdl(paged_decode_combine_kernel<QT, D, G>, dim3(units), dim3(combine_threads<D, G>()), 0,
+                               stream, p, grid),
+                    "paged_decode_combine_kernel launch"))
+      return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
@@ -86,13 +115,26 @@ DecodeLauncher decode_launcher_f16(int head_dim, int group);
 DecodeLauncher decode_launcher_bf16(int head_dim, int group);
 DecodeLauncher decode_launcher_e4m3(int q_dtype, int head_dim, int group);
 
+constexpr int kCoreWarps = 8;   // consumer warps of the CUDA-core variant
+constexpr int kMmaWarps = 4;    // consumer warps of the tensor-core variant
+
+// G = 1 uses the CUDA-core consumer; G >= 2 over a 16-bit cache uses the
+// tensor-core consumer (the q-group times a 16-token block is an MMA tile).
+template <typename QT, typename KV, int D, int G>
+DecodeLauncher pick_variant() {
+  if constexpr (G >= 2 && KV::kBytes == 2)
+    return launch_decode_variant<QT, KV, D, G, kMmaWarps, true>;
+  else
+    return launch_decode_variant<QT, KV, D, G, kCoreWarps, false>;
+}
+
 template <typename QT, typename KV, int D>
 DecodeLauncher pick_group(int group) {
   switch (group) {
-    case 1: return launch_decode_variant<QT, KV, D, 1, 8>;
-    case 2: return launch_decode_variant<QT, KV, D, 2, 8>;
-    case 4: return launch_decode_variant<QT, KV, D, 4, 8>;
-    case 8: return launch_decode_variant<QT, KV, D, 8, 8>;
+    case 1: return pick_variant<QT, KV, D, 1>();
+    case 2: return pick_variant<QT, KV, D, 2>();
+    case 4: return pick_variant<QT, KV, D, 4>();
+    case 8: return pick_variant<QT, KV, D, 8>();
     default: return nullptr;
   }
 }

@@ -140,6 +140,17 @@ __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, 
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: kernels of one decode step are launched so
+// that the next kernel's launch overlaps this one's tail.  Every kernel waits
+// for its predecessor's completion (and memory) before it reads global data,
+// then lets its own successor start launching.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // element conversions
 // ---------------------------------------------------------------------------
 struct F16 {
