@@ -18,7 +18,8 @@
 // merges the partials of each (sequence, KV head) by log-sum-exp.
 //
 // Thread block.  NW consumer warps + 1 producer warp.  The producer walks the
-// segments, reads block ids from the table (32 at a time, one per lane) and
+// segments, reads block ids from the table (32 at a time, one per lane; each
+// lane then issues the copies of its own block, many lanes at once) and
 // stages each (block, KV head) slab of K and of V -- [16, head_dim], contiguous
 // in the (num_blocks, H_kv, 16, head_dim) layout -- into shared memory with
 // TMA: one 1-D bulk copy per slab (linear layout), or, for the tensor-core
@@ -31,11 +32,12 @@
 //
 // Consumers.  Scores are kept in the log2 domain (scale * log2(e) applied in
 // fp32), so exponentials are exp2.
-//  * CUDA-core consumer (G = 1, E4M3 cache): a token row is split over
+//  * CUDA-core consumer (G = 1; E4M3 with 64-byte rows): a token row is split over
 //    LPT = D / 8 lanes; partial dot products are reduced by a butterfly
 //    reduce-scatter; p is shared through a per-warp scratch row; p.V
 //    accumulates in fp32 registers, each lane owning 8 output elements.
-//  * Tensor-core consumer (G >= 2, 16-bit cache): q.K^T of a block is one
+//  * Tensor-core consumer (G >= 2; 16-bit cache, or E4M3 with 128-byte rows
+//    converted to f16 in registers): q.K^T of a block is one
 //    mma.m16n8k16 per 16 head_dim elements with the 16 tokens as M and the G
 //    query heads (zero-padded to 8) as N; the fp32 scores of the C fragment
 //    go through the online softmax in registers; p is rounded to the cache's
@@ -46,6 +48,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "pkv_common.cuh"
 
@@ -121,7 +125,8 @@ struct DecodeTraits {
   static constexpr int kNV = kTPG * G;                         // partial scores per lane
   static constexpr int kNF = (kNV >= kLPT) ? kNV / kLPT : 1;   // held scores after reduce-scatter
   static_assert(kNF == (G >= 2 ? G / 2 : 1), "lane/head mapping");
-  static_assert(!MMA || (G >= 2 && G <= 8 && kEsz == 2 && (D * kEsz) % 128 == 0), "tensor-core variant");
+  static_assert(!MMA || (G >= 2 && G <= 8 && (D * kEsz) % 128 == 0 && (kEsz == 2 || D * kEsz == 128)),
+                "tensor-core variant");
 
   // shared memory layout (byte offsets from a 1024-byte aligned base)
   static __host__ __device__ size_t q_off(int stages) { return static_cast<size_t>(stages) * kStage; }
@@ -212,6 +217,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, BF16) {
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, F16) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// two E4M3 codes (bits 0-15 of w: low byte first) -> packed f16x2, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(w & 0xffffu)));
   return r;
 }
 
@@ -370,26 +381,35 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
         }
         __syncwarp();
         ++j;
-        // stream the segment's K/V slabs
+        // Stream the segment's K/V slabs.  Lane j of the producer warp owns
+        // block j of each 32-block window of the table (its table entry is
+        // loaded by that lane, one window ahead).  The window is issued in
+        // sub-batches of min(S, 32) blocks: the blocks of a sub-batch occupy
+        // distinct stages, so their lanes wait and issue in parallel; the
+        // __syncwarp between sub-batches keeps each stage's uses in order.
         const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+        const int sub = S < 32 ? S : 32;
         int ids = (i0 + lane < i1) ? row[i0 + lane] : 0;
         for (int ib = i0; ib < i1; ib += 32) {
-          const int nxt = (ib + 32 + lane < i1) ? row[ib + 32 + lane] : 0;   // prefetch the next 32
+          const int nxt = (ib + 32 + lane < i1) ? row[ib + 32 + lane] : 0;   // prefetch the next window
           const int cnt = min(32, i1 - ib);
-          for (int jj = 0; jj < cnt; ++jj) {
-            const int pid = __shfl_sync(0xffffffffu, ids, jj);
-            if (lane == 0) {
-              const uint32_t jw = k / NW;                       // this block's index in its warp's ring
-              const int s = static_cast<int>(k % NW) + NW * static_cast<int>(jw % SPW);
+          for (int sb = 0; sb < cnt; sb += sub) {
+            if (lane >= sb && lane < min(sb + sub, cnt) && !*abort_flag) {
+              const uint32_t kk = k + lane;                        // CTA-local block counter
+              const uint32_t jw = kk / NW;                         // index in its warp's ring
+              const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
               const uint32_t use = jw / SPW;
-              if (use >= 1 && !*abort_flag && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.err)) *abort_flag = 1;
-              const bool ok = pid >= 0 && pid < p.num_blocks && !*abort_flag;
+              bool ok = ids >= 0 && ids < p.num_blocks;
+              if (use >= 1 && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.err)) {
+                *abort_flag = 1;
+                ok = false;
+              }
               stage_ok[s] = ok ? 1 : 0;
               unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
               if (ok) {
                 mbar_arrive_expect_tx(&full_bar[s], T::kStage);
                 if constexpr (MMA) {
-                  const int y = (pid * Hkv + g) * kBlockSize;
+                  const int y = (ids * Hkv + g) * kBlockSize;
 #pragma unroll
                   for (int t = 0; t < T::kSubTiles; ++t) {
                     tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
@@ -397,7 +417,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
                                 pol_stream);
                   }
                 } else {
-                  const int64_t slab = (static_cast<int64_t>(pid) * Hkv + g) * T::kSlab;
+                  const int64_t slab = (static_cast<int64_t>(ids) * Hkv + g) * T::kSlab;
                   bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
                   bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
                 }
@@ -406,10 +426,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
                 mbar_arrive(&full_bar[s]);
               }
             }
-            ++k;
+            __syncwarp();
           }
+          k += cnt;
           ids = nxt;
-          __syncwarp();
         }
         f = f_end;
       }
@@ -467,14 +487,33 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
 
     if constexpr (MMA) {
       // ------------------------- tensor-core consumer -------------------------
+      // MT: operand type of the MMAs.  A 16-bit cache multiplies in its own
+      // type.  An E4M3 cache is converted to f16 in registers (every E4M3
+      // value is exact in f16) and q is converted to f16 (exact in f16's
+      // normal range); fp8 rows are 128 bytes, one swizzled sub-tile.
+      constexpr bool kFp8 = (T::kEsz == 1);
+      using MT = std::conditional_t<kFp8, F16, QT>;
       constexpr int KS = D / 16;
       uint32_t bq[KS][2];
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
+      {
         const bool live = r4 < G;
-        const unsigned char* qh = qrow + ((live ? r4 : 0) * D + 16 * ks + 2 * q4) * 2;
-        bq[ks][0] = live ? *reinterpret_cast<const uint32_t*>(qh) : 0u;
-        bq[ks][1] = live ? *reinterpret_cast<const uint32_t*>(qh + 16) : 0u;
+        const int hq = live ? r4 : 0;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          if constexpr (kFp8) {
+            // k-step ks covers head_dim [16 ks, 16 ks + 16) in the order the
+            // converted fp8 A fragments use: k = 2 q4 + {0,1} <-> d = 16 ks + 4 q4 + {0,1},
+            // k = 2 q4 + 8 + {0,1} <-> d = 16 ks + 4 q4 + {2,3}
+            const uint2 raw = *reinterpret_cast<const uint2*>(qrow + (hq * D + 16 * ks + 4 * q4) * 2);
+            const float2 lo = unpack2(raw.x, QT{}), hi = unpack2(raw.y, QT{});
+            bq[ks][0] = live ? pack2(lo.x, lo.y, F16{}) : 0u;
+            bq[ks][1] = live ? pack2(hi.x, hi.y, F16{}) : 0u;
+          } else {
+            const unsigned char* qh = qrow + (hq * D + 16 * ks + 2 * q4) * 2;
+            bq[ks][0] = live ? *reinterpret_cast<const uint32_t*>(qh) : 0u;
+            bq[ks][1] = live ? *reinterpret_cast<const uint32_t*>(qh + 16) : 0u;
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty_bar[qs]);
@@ -482,8 +521,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      const int krow = mrow + 8 * (mi & 1), kchunk = mi >> 1;   // A of q.K^T
-      const int vrow = mrow + 8 * (mi >> 1), vchunk = mi & 1;   // A of p.V (transposed load)
+      const int krow = mrow + 8 * (mi & 1), kchunk = mi >> 1;   // A of q.K^T (and fp8 V)
+      const int vrow = mrow + 8 * (mi >> 1), vchunk = mi & 1;   // A of p.V (16-bit transposed load)
       for (int ii = first; ii < nseg; ii += NW) {
         const uint32_t kk = k_base + ii;
         const uint32_t jw = kk / NW;
@@ -497,11 +536,25 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
         const uint32_t kslab = smem_u32(ring + static_cast<size_t>(s) * T::kStage);
         const uint32_t vslab = kslab + T::kSlab;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (kFp8) {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a[4];
-          ldsm_x4(swz_addr(kslab, krow, 2 * ks + kchunk), a);
-          mma16816(c, a, bq[ks][0], bq[ks][1], QT{});
+          for (int cp = 0; cp < KS / 2; ++cp) {
+            uint32_t r[4];   // (tokens 0-7, chunk 2cp), (8-15, 2cp), (0-7, 2cp+1), (8-15, 2cp+1)
+            ldsm_x4(swz_addr(kslab, krow, 2 * cp + kchunk), r);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t a[4] = {e4m3x2_to_f16x2(r[2 * h2]), e4m3x2_to_f16x2(r[2 * h2 + 1]),
+                                     e4m3x2_to_f16x2(r[2 * h2] >> 16), e4m3x2_to_f16x2(r[2 * h2 + 1] >> 16)};
+              mma16816(c, a, bq[2 * cp + h2][0], bq[2 * cp + h2][1], F16{});
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(swz_addr(kslab, krow, 2 * ks + kchunk), a);
+            mma16816(c, a, bq[ks][0], bq[ks][1], MT{});
+          }
         }
         const bool v0 = r4 < n_valid, v1 = r4 + 8 < n_valid;
         const float s00 = v0 ? c[0] * sc : -INFINITY, s01 = v0 ? c[1] * sc : -INFINITY;
@@ -515,9 +568,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0, ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
         const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
-        const uint32_t x0 = pack2(exp2f(s00 - ref0), exp2f(s01 - ref1), QT{});   // tokens 0..7
-        const uint32_t x1 = pack2(exp2f(s10 - ref0), exp2f(s11 - ref1), QT{});   // tokens 8..15
-        const float2 p0 = unpack2(x0, QT{}), p1 = unpack2(x1, QT{});
+        const uint32_t x0 = pack2(exp2f(s00 - ref0), exp2f(s01 - ref1), MT{});   // tokens 0..7
+        const uint32_t x1 = pack2(exp2f(s10 - ref0), exp2f(s11 - ref1), MT{});   // tokens 8..15
+        const float2 p0 = unpack2(x0, MT{}), p1 = unpack2(x1, MT{});
         l0 = l0 * a0 + (p0.x + p1.x);
         l1 = l1 * a1 + (p0.y + p1.y);
         const bool resc = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
@@ -530,11 +583,29 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
             o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
           }
         }
+        if constexpr (kFp8) {
+          // V rows converted to f16 and transposed in registers: m-tile c's row
+          // r < 8 is d = 16c + 4(r/2) + r%2, row r + 8 is that d + 2
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          uint32_t a[4];
-          ldsm_x4_trans(swz_addr(vslab, vrow, 2 * mt + vchunk), a);
-          mma16816(o[mt], a, b0, b1, QT{});
+          for (int cp = 0; cp < KS / 2; ++cp) {
+            uint32_t r[4];
+            ldsm_x4(swz_addr(vslab, krow, 2 * cp + kchunk), r);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t a[4] = {movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2])),
+                                     movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2] >> 16)),
+                                     movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2 + 1])),
+                                     movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2 + 1] >> 16))};
+              mma16816(o[2 * cp + h2], a, b0, b1, F16{});
+            }
+          }
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(swz_addr(vslab, vrow, 2 * mt + vchunk), a);
+            mma16816(o[mt], a, b0, b1, MT{});
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -549,10 +620,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
       if (h0 < G) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          mw[h0 * D + 16 * mt + r4] = o[mt][0];
-          mw[(h0 + 1) * D + 16 * mt + r4] = o[mt][1];
-          mw[h0 * D + 16 * mt + r4 + 8] = o[mt][2];
-          mw[(h0 + 1) * D + 16 * mt + r4 + 8] = o[mt][3];
+          const int d_lo = kFp8 ? 16 * mt + 4 * (r4 >> 1) + (r4 & 1) : 16 * mt + r4;
+          const int d_hi = kFp8 ? d_lo + 2 : d_lo + 8;
+          mw[h0 * D + d_lo] = o[mt][0];
+          mw[(h0 + 1) * D + d_lo] = o[mt][1];
+          mw[h0 * D + d_hi] = o[mt][2];
+          mw[(h0 + 1) * D + d_hi] = o[mt][3];
         }
         if (r4 == 0) {
           mw[G * D + h0] = m0;

@@ -63,7 +63,10 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
                   "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  occ = std::min(occ, li.max_ctas_per_sm);
+  // resident blocks per SM: measured best on GB300 at 2 for the CUDA-core
+  // variant (8 consumer warps each) and at the register limit (3) for the
+  // tensor-core variant (4 consumer warps each)
+  occ = std::min(occ, std::min(li.max_ctas_per_sm, MMA ? 4 : 2));
   int spw = 1;
   if (li.stages > 0) {
     spw = std::max(1, li.stages / NW);
@@ -84,7 +87,7 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
                   "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  occ = std::min(occ, li.max_ctas_per_sm);
+  occ = std::min(occ, std::min(li.max_ctas_per_sm, MMA ? 4 : 2));
   int grid = li.num_sms * occ;
   if (p.part_blocks > 0 && li.part_ranges_cap < grid) grid = static_cast<int>(li.part_ranges_cap);
   if (grid < 1) grid = 1;
@@ -118,11 +121,12 @@ DecodeLauncher decode_launcher_e4m3(int q_dtype, int head_dim, int group);
 constexpr int kCoreWarps = 8;   // consumer warps of the CUDA-core variant
 constexpr int kMmaWarps = 4;    // consumer warps of the tensor-core variant
 
-// G = 1 uses the CUDA-core consumer; G >= 2 over a 16-bit cache uses the
-// tensor-core consumer (the q-group times a 16-token block is an MMA tile).
+// G = 1 uses the CUDA-core consumer; G >= 2 over a 16-bit cache, or over an
+// E4M3 cache with 128-byte rows, uses the tensor-core consumer (the q-group
+// times a 16-token block is an MMA tile).
 template <typename QT, typename KV, int D, int G>
 DecodeLauncher pick_variant() {
-  if constexpr (G >= 2 && KV::kBytes == 2)
+  if constexpr (G >= 2 && (KV::kBytes == 2 || D * KV::kBytes == 128))
     return launch_decode_variant<QT, KV, D, G, kMmaWarps, true>;
   else
     return launch_decode_variant<QT, KV, D, G, kCoreWarps, false>;

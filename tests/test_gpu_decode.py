@@ -148,6 +148,20 @@ def test_fp8_small(pkv, partition):
     _check(case, gu.oracle_decode(w, kp, vp), fp8=True, label=f"fp8 P={partition}")
 
 
+@pytest.mark.parametrize("hq,hkv,head_dim", [(16, 8, 128), (16, 16, 128), (64, 8, 128), (8, 4, 64), (8, 8, 64),
+                                             (16, 2, 64)])
+def test_fp8_shapes(pkv, hq, hkv, head_dim):
+    # every group size on both head dims: the tensor-core consumer (128-byte
+    # rows, G >= 2) and the CUDA-core consumer (G = 1 or 64-byte rows)
+    w = wl.build("fp8shape", batch=4, n_q_heads=hq, n_kv_heads=hkv, head_dim=head_dim, dtype="f16",
+                 kv_dtype="e4m3", context_lens=[1, 33, 250, 401], seed=hq * 7 + hkv + head_dim)
+    kc, vc, kn, vn = gu.oracle_fp8_codes(w)
+    case = gu.GpuCase(w, codes=(kc, vc))
+    case.step(partition_tokens=0)
+    kp, vp = gu.oracle_pools_after_append(w)
+    _check(case, gu.oracle_decode(w, kp, vp), fp8=True, label=f"fp8 {hq}/{hkv} d{head_dim}")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
