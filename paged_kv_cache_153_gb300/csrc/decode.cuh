@@ -864,22 +864,32 @@ __global__ void __launch_bounds__(combine_threads<D, G>())
   const bool first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
   const int h = (4 * t) / D, e = (4 * t) % D;
   float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
-  for (int64_t r = r0; r <= r1; ++r) {
-    // ranges between r0 and r1 may be empty (fewer blocks than ranges): they
-    // wrote nothing for this (b, g) and are skipped
-    if (range_start(r + 1, W, R, p.part_blocks) <= range_start(r, W, R, p.part_blocks)) continue;
-    const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
-    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2);
-    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e);
-    const float mn = fmaxf(M, ml.x);
-    const float ref = (mn == -INFINITY) ? 0.f : mn;
-    const float a = exp2f(M - ref), w = exp2f(ml.x - ref);
-    L = L * a + w * ml.y;
-    O0 = O0 * a + w * o.x;
-    O1 = O1 * a + w * o.y;
-    O2 = O2 * a + w * o.z;
-    O3 = O3 * a + w * o.w;
-    M = mn;
+  constexpr int kBatch = 8;   // partials whose loads are issued together
+  for (int64_t rb = r0; rb <= r1; rb += kBatch) {
+    float2 ml[kBatch];
+    float4 ov[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int64_t r = rb + q;
+      // ranges between r0 and r1 may be empty (fewer blocks than ranges):
+      // they wrote nothing for this (b, g)
+      const bool live = r <= r1 && range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
+      const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
+      ml[q] = live ? *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2) : make_float2(-INFINITY, 0.f);
+      ov[q] = live ? *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const float mn = fmaxf(M, ml[q].x);
+      const float ref = (mn == -INFINITY) ? 0.f : mn;
+      const float a = exp2f(M - ref), w = exp2f(ml[q].x - ref);
+      L = L * a + w * ml[q].y;
+      O0 = O0 * a + w * ov[q].x;
+      O1 = O1 * a + w * ov[q].y;
+      O2 = O2 * a + w * ov[q].z;
+      O3 = O3 * a + w * ov[q].w;
+      M = mn;
+    }
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   store4(O0 * inv, O1 * inv, O2 * inv, O3 * inv);

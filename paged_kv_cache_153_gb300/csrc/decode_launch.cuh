@@ -90,6 +90,13 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   occ = std::min(occ, std::min(li.max_ctas_per_sm, MMA ? 4 : 2));
   int grid = li.num_sms * occ;
   if (p.part_blocks > 0 && li.part_ranges_cap < grid) grid = static_cast<int>(li.part_ranges_cap);
+  // a small workload (upper bound on blocks known from max_context_len) needs
+  // no more than one thread block per few blocks of work
+  if (p.part_blocks == 0) {
+    const int64_t w_max = static_cast<int64_t>(p.batch) * p.n_kv_heads *
+                          std::min<int64_t>(p.max_blocks_per_seq, p.max_nblk);
+    grid = static_cast<int>(std::min<int64_t>(grid, std::max<int64_t>(1, (w_max + 3) / 4)));
+  }
   if (grid < 1) grid = 1;
   p.stages = stages;
   li.grid = grid;
