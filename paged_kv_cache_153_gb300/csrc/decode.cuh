@@ -823,22 +823,31 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
 // ---------------------------------------------------------------------------
 // combine: out[b, g*G + h] = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r over
 // the partial slots of (b, g); zeros for an empty context.  One thread block
-// per (b, g), one thread per 4 consecutive outputs, one online pass over the
-// partials; (b, g) pairs written directly by the decode kernel are skipped.
+// per (b, g).  Each group of kSplit adjacent lanes owns 4 consecutive outputs;
+// lane s of the group merges pieces s, s + kSplit, ... (loads issued 4 at a
+// time), then the group combines its states with xor shuffles.  (b, g) pairs
+// written directly by the decode kernel are skipped.
 // ---------------------------------------------------------------------------
-template <int D, int G>
-constexpr int combine_threads() {
-  return (G * D / 4) < 32 ? 32 : (G * D / 4);
+// WIDE: 8 lanes per output quad (4 when that exceeds 1024 threads) for
+// (sequence, KV head) pairs split into many pieces; else one lane per quad.
+template <int D, int G, bool WIDE>
+__host__ __device__ constexpr int combine_split() {
+  return !WIDE ? 1 : ((G * D / 4) * 8 <= 1024 ? 8 : 4);
+}
+template <int D, int G, bool WIDE>
+__host__ __device__ constexpr int combine_threads() {
+  return (G * D / 4) * combine_split<D, G, WIDE>() < 32 ? 32 : (G * D / 4) * combine_split<D, G, WIDE>();
 }
 
-template <typename QT, int D, int G>
-__global__ void __launch_bounds__(combine_threads<D, G>())
+template <typename QT, int D, int G, bool WIDE>
+__global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
     paged_decode_combine_kernel(const __grid_constant__ DecodeParams p, int grid_ranges) {
+  constexpr int kSplit = combine_split<D, G, WIDE>();
   pdl_wait_and_release();
   const int u = blockIdx.x;
   const int b = u / p.n_kv_heads, g = u % p.n_kv_heads;
-  const int t = threadIdx.x;
-  if (t >= G * D / 4) return;
+  const int t = threadIdx.x / kSplit, sub = threadIdx.x % kSplit;
+  const bool live_t = t < G * D / 4;
   auto* out = static_cast<typename QT::storage*>(p.out);
   const int c0 = p.ws_cum[b], c1 = p.ws_cum[b + 1];
   const int nb = c1 - c0;
@@ -848,7 +857,7 @@ __global__ void __launch_bounds__(combine_threads<D, G>())
     *reinterpret_cast<uint2*>(out + base_out) = make_uint2(lo, hi);
   };
   if (nb == 0) {
-    store4(0.f, 0.f, 0.f, 0.f);
+    if (live_t && sub == 0) store4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int64_t W = static_cast<int64_t>(p.n_kv_heads) * p.ws_cum[p.batch];
@@ -862,18 +871,19 @@ __global__ void __launch_bounds__(combine_threads<D, G>())
   const int64_t r0 = range_of(S0), r1 = range_of(E0 - 1);
   if (r0 == r1) return;   // one segment: written by the decode kernel
   const bool first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
-  const int h = (4 * t) / D, e = (4 * t) % D;
+  const int h = live_t ? (4 * t) / D : 0, e = live_t ? (4 * t) % D : 0;
   float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
-  constexpr int kBatch = 8;   // partials whose loads are issued together
-  for (int64_t rb = r0; rb <= r1; rb += kBatch) {
+  constexpr int kBatch = WIDE ? 4 : 8;   // partials whose loads are issued together, per lane
+  for (int64_t rb = r0 + sub; rb <= r1; rb += kBatch * kSplit) {
     float2 ml[kBatch];
     float4 ov[kBatch];
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
-      const int64_t r = rb + q;
+      const int64_t r = rb + static_cast<int64_t>(q) * kSplit;
       // ranges between r0 and r1 may be empty (fewer blocks than ranges):
       // they wrote nothing for this (b, g)
-      const bool live = r <= r1 && range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
+      const bool live = live_t && r <= r1 &&
+                        range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
       const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
       ml[q] = live ? *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2) : make_float2(-INFINITY, 0.f);
       ov[q] = live ? *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -891,8 +901,31 @@ __global__ void __launch_bounds__(combine_threads<D, G>())
       M = mn;
     }
   }
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  store4(O0 * inv, O1 * inv, O2 * inv, O3 * inv);
+  // combine the kSplit lane states of each output quad
+#pragma unroll
+  for (int msk = 1; msk < kSplit; msk <<= 1) {
+    // (kSplit = 1: no exchange)
+    const float Mo = __shfl_xor_sync(0xffffffffu, M, msk), Lo = __shfl_xor_sync(0xffffffffu, L, msk);
+    const float A0 = __shfl_xor_sync(0xffffffffu, O0, msk), A1 = __shfl_xor_sync(0xffffffffu, O1, msk);
+    const float A2 = __shfl_xor_sync(0xffffffffu, O2, msk), A3 = __shfl_xor_sync(0xffffffffu, O3, msk);
+    const float mn = fmaxf(M, Mo);
+    const float ref = (mn == -INFINITY) ? 0.f : mn;
+    const float a = exp2f(M - ref), w = exp2f(Mo - ref);
+    // combine in a lane-order independent way: the lower lane's state first
+    const bool low = (sub & msk) == 0;
+    const float as = low ? a : w, ws = low ? w : a;
+    L = (low ? L : Lo) * as + (low ? Lo : L) * ws;
+    const float n0 = (low ? O0 : A0) * as + (low ? A0 : O0) * ws;
+    const float n1 = (low ? O1 : A1) * as + (low ? A1 : O1) * ws;
+    const float n2 = (low ? O2 : A2) * as + (low ? A2 : O2) * ws;
+    const float n3 = (low ? O3 : A3) * as + (low ? A3 : O3) * ws;
+    O0 = n0; O1 = n1; O2 = n2; O3 = n3;
+    M = mn;
+  }
+  if (live_t && sub == 0) {
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    store4(O0 * inv, O1 * inv, O2 * inv, O3 * inv);
+  }
 }
 
 }  // namespace pkv

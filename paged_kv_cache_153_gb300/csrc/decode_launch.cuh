@@ -112,10 +112,15 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
     return PKV_ERR_CUDA;
   const int units = p.batch * p.n_kv_heads;
   if (units > 0) {
-    if (cuda_failed(launch_pdl(paged_decode_combine_kernel<QT, D, G>, dim3(units), dim3(combine_threads<D, G>()), 0,
-                               stream, p, grid),
-                    "paged_decode_combine_kernel launch"))
-      return PKV_ERR_CUDA;
+    // fixed partitions of long contexts give many pieces per (sequence, KV
+    // head): merge those with several lanes per output
+    const bool wide = p.part_blocks > 0 && (p.max_nblk + p.part_blocks - 1) / p.part_blocks >= 16;
+    const cudaError_t e =
+        wide ? launch_pdl(paged_decode_combine_kernel<QT, D, G, true>, dim3(units),
+                          dim3(combine_threads<D, G, true>()), 0, stream, p, grid)
+             : launch_pdl(paged_decode_combine_kernel<QT, D, G, false>, dim3(units),
+                          dim3(combine_threads<D, G, false>()), 0, stream, p, grid);
+    if (cuda_failed(e, "paged_decode_combine_kernel launch")) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
