@@ -152,6 +152,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# replicas: every rank runs its own copy of the workload; no data crosses ranks
+# ---------------------------------------------------------------------------
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's time (the job ends when its last replica ends)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest time."""
+    return world * units_per_rank / seconds
+
+
+# ---------------------------------------------------------------------------
 # oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_step(w: wl.Workload, seqs) -> int:
@@ -332,9 +350,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dist, dev if dist.get_backend() == "nccl" else "cpu")
 
     # ---- end to end through the host-buffer entry point ---------------------
     pin = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a)).view(t16[dt]) if dt else
@@ -361,12 +377,10 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
             host_step()
         e2e_s = time.perf_counter() - t0
         if dist is not None:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+            e2e_s = max_over_ranks(e2e_s, dist, dev if dist.get_backend() == "nccl" else "cpu")
         log("end-to-end loop done")
         h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_t, h_l))
-        e2e = {"value": world * w.batch * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": replica_throughput(w.batch * n_e2e, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": n_e2e,
                "path": "pkv_decode_step_host (pinned host buffers in, result read back every step)"}
 
@@ -375,7 +389,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     peak, peak_kind = measured_peak()
     algo = w.algorithmic_bytes()
     achieved = algo / (dec_avg_ms * 1e-3) / 1e9
-    value = world * w.batch * args.steps / (elapsed_ms * 1e-3)
+    value = replica_throughput(w.batch * args.steps, world, elapsed_ms * 1e-3)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
