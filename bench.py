@@ -57,7 +57,7 @@ def describe(w: wl.Workload) -> dict:
         "batch": w.batch, "num_q_heads": w.n_q_heads, "num_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
         "kv_dtype": w.kv_dtype, "block_size": 16, "num_blocks": w.num_blocks,
         "context_tokens_total": int(ctx.sum()), "partition_tokens": w.partition_tokens,
-        "step": "slot mapping + kv_append + paged decode attention (split + combine)",
+        "step": "pkv_paged_decode_step: slot mapping + append + paged decode attention in one decode launch, + combine",
         "l2": f"inputs larger than L2: {w.algorithmic_bytes() / 1e9:.3f} GB of KV + q + out per step, no flush",
     }
 
@@ -286,31 +286,23 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         stream.synchronize()
     log("inputs resident on the device")
 
-    def attention():
-        if fp8:
-            pkv.pkv_paged_decode_attention_fp8(q, k_cache, v_cache, ks, vs, tables, lens, out, scale=w.scale,
-                                               max_context_len=max_ctx, workspace=ws,
-                                               partition_tokens=w.partition_tokens, err_flag=err,
-                                               stream=stream)
-        else:
-            pkv.pkv_paged_decode_attention(q, k_cache, v_cache, tables, lens, out, scale=w.scale,
-                                           max_context_len=max_ctx, workspace=ws,
-                                           partition_tokens=w.partition_tokens, err_flag=err, stream=stream)
-
     def step(ev0=None, ev1=None):
-        pkv.pkv_slot_mapping(tables, lens, slots, num_blocks=w.num_blocks, position_offset=-1, err_flag=err,
-                             stream=stream)
-        if fp8:
-            pkv.pkv_kv_append_fp8(k_new, v_new, slots, k_cache, v_cache, ks, vs, err_flag=err, stream=stream)
-        else:
-            pkv.pkv_kv_append(k_new, v_new, slots, k_cache, v_cache, err_flag=err, stream=stream)
+        # one fused call: slot mapping + append + attention (decode kernel), then the partial merge
         if ev0 is not None:
             ev0.record(stream)
-        attention()
+        if fp8:
+            pkv.pkv_paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, ks, vs, tables, lens, out,
+                                          scale=w.scale, max_context_len=max_ctx, workspace=ws,
+                                          partition_tokens=w.partition_tokens, slot_mapping_out=slots,
+                                          err_flag=err, stream=stream)
+        else:
+            pkv.pkv_paged_decode_step(q, k_new, v_new, k_cache, v_cache, tables, lens, out, scale=w.scale,
+                                      max_context_len=max_ctx, workspace=ws, partition_tokens=w.partition_tokens,
+                                      slot_mapping_out=slots, err_flag=err, stream=stream)
         if ev1 is not None:
             ev1.record(stream)
 
-    launches_per_step = 4          # slot mapping, append, decode, combine
+    launches_per_step = 2          # decode (with slot mapping and append), combine
 
     dist = None
     if world > 1:
@@ -387,7 +379,8 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     if rank != 0:
         return None
     peak, peak_kind = measured_peak()
-    algo = w.algorithmic_bytes()
+    # attention's KV + q + out, plus the appended rows written to the cache
+    algo = w.algorithmic_bytes() + 2 * w.batch * w.n_kv_heads * w.head_dim * w.kv_elt_bytes
     achieved = algo / (dec_avg_ms * 1e-3) / 1e9
     value = replica_throughput(w.batch * args.steps, world, elapsed_ms * 1e-3)
     res = {
@@ -397,7 +390,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         "config": dict(describe(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-                     "kernel": "pkv_paged_decode_attention call (decode + combine kernels)",
+                     "kernel": "pkv_paged_decode_step call (decode kernel with slot mapping and append, then the combine kernel)",
                      "algorithmic_bytes_per_launch": algo, "avg_launch_ms": dec_avg_ms,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "frac_of_8TBps": achieved / 8000.0},

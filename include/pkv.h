@@ -206,12 +206,45 @@ pkv_status pkv_paged_decode_attention_fp8(const void* q, const uint8_t* k_cache,
                                           void* stream);
 
 /* ---------------------------------------------------------------------------
+ * One whole decode step in a single decode launch (plus the partial merge):
+ * for every sequence b, append k_new[b] / v_new[b] at position
+ * p = context_lens[b] - 1 (slot = block_tables[b][p / 16] * 16 + p % 16,
+ * written to slot_mapping_out[b] when that pointer is not NULL; -1 for an
+ * empty context or an out-of-range table entry), then attend
+ * over the context_lens[b] tokens.  Same results as pkv_slot_mapping +
+ * pkv_kv_append + pkv_paged_decode_attention, bit for bit.
+ *   k_new, v_new    device [batch, num_kv_heads, head_dim] in dtype.
+ *   k_cache, v_cache written (the new rows) and read.
+ * The new row's slot must belong to sequence b alone (not a block shared with
+ * another table), as for any append.  Other arguments as in
+ * pkv_paged_decode_attention.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                 const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale,
+                                 void* out, pkv_dtype dtype, int partition_tokens, int64_t* slot_mapping_out,
+                                 void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The same fused step over an E4M3 cache: the new rows (q_dtype) are stored as
+ * E4M3_RN_satfinite(fl32(x) / scale[h]) exactly as pkv_kv_append_fp8 stores
+ * them, and attention uses those codes, as pkv_paged_decode_attention_fp8.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_step_fp8(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
+                                     uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                                     const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                     int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale,
+                                     void* out, pkv_dtype q_dtype, int partition_tokens, int64_t* slot_mapping_out,
+                                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * One whole decode step from HOST buffers: copies q, k_new, v_new,
  * block_tables and context_lens from (preferably pinned) host memory into the
- * caller's device staging buffers, computes the slots of the new tokens
- * (position context_lens[b] - 1 of sequence b), appends k_new / v_new, runs
- * paged decode attention and copies out back to host memory, all enqueued on
- * `stream`.  The caller synchronises the stream before reading h_out.
+ * caller's device staging buffers, runs pkv_paged_decode_step (slots of the
+ * new tokens into d_slots, append, attention) and copies out back to host
+ * memory, all enqueued on `stream`.  The caller synchronises the stream before reading h_out.
  *   h_*        host pointers; shapes as above with num_tokens = batch.
  *   d_*        device staging buffers of the same sizes; d_slots is int64 [batch].
  *   caches     device, persistent across steps.

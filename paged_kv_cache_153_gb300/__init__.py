@@ -20,7 +20,7 @@ __all__ = [
     "PKV_F16", "PKV_BF16", "PkvError", "lib", "library_path",
     "pkv_slot_mapping", "pkv_kv_append", "pkv_kv_append_fp8", "pkv_decode_workspace_bytes",
     "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8", "pkv_decode_step_host",
-    "pkv_paged_decode_attention_noalloc",
+    "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_step", "pkv_paged_decode_step_fp8",
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
 ]
 
@@ -47,6 +47,10 @@ _SIGS = {
                                         _p, _sz, _p, _p]),
     "pkv_paged_decode_attention_fp8": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f,
                                             _p, _i, _i, _p, _sz, _p, _p]),
+    "pkv_paged_decode_step": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i, _i, _p,
+                                   _p, _sz, _p, _p]),
+    "pkv_paged_decode_step_fp8": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p,
+                                       _i, _i, _p, _p, _sz, _p, _p]),
     "pkv_paged_decode_attention_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
                                                 _i, _p, _p]),
     "pkv_decode_step_host": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i,
@@ -172,6 +176,30 @@ def pkv_paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_
         _ptr(context_lens), b, hq, hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale, _ptr(out),
         _dtype_code(q, q_dtype), partition_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, *, scale: float,
+                          max_context_len: int, workspace, partition_tokens: int = 0, slot_mapping_out=None,
+                          dtype=None, err_flag=None, stream=None) -> None:
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_decode_step", lib.pkv_paged_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), b,
+        hq, hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale, _ptr(out), _dtype_code(q, dtype),
+        partition_tokens, _ptr(slot_mapping_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                              out, *, scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                              slot_mapping_out=None, q_dtype=None, err_flag=None, stream=None) -> None:
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_decode_step_fp8", lib.pkv_paged_decode_step_fp8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(context_lens), b, hq, hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale,
+        _ptr(out), _dtype_code(q, q_dtype), partition_tokens, _ptr(slot_mapping_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
 
 
 def pkv_paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, out, *, scale: float,

@@ -115,7 +115,8 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
                          int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale, void* out,
                          pkv_dtype dtype, int partition_tokens, void* workspace, size_t workspace_bytes,
-                         int32_t* err_flag, void* stream) {
+                         int32_t* err_flag, void* stream, const void* k_new = nullptr, const void* v_new = nullptr,
+                         int64_t* slots_out = nullptr) {
   if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks < 0 ||
       max_context_len < 0 || partition_tokens < 0 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
@@ -131,6 +132,8 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
     return PKV_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
   const int num_sms = sm_count();
   if (num_sms <= 0) return PKV_ERR_CUDA;
   WsLayout w;
@@ -155,6 +158,9 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slots_out = slots_out;
   p.ws_cum = reinterpret_cast<int32_t*>(ws + w.cum_off);
   p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
   p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
@@ -240,6 +246,36 @@ extern "C" pkv_status pkv_paged_decode_attention_fp8(const void* q, const uint8_
                        err_flag, stream);
 }
 
+extern "C" pkv_status pkv_paged_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                            void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                            int max_context_len, float scale, void* out, pkv_dtype dtype,
+                                            int partition_tokens, int64_t* slot_mapping_out, void* workspace,
+                                            size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  return decode_common(false, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       max_context_len, scale, out, dtype, partition_tokens, workspace, workspace_bytes, err_flag,
+                       stream, k_new, v_new, slot_mapping_out);
+}
+
+extern "C" pkv_status pkv_paged_decode_step_fp8(const void* q, const void* k_new, const void* v_new,
+                                                uint8_t* k_cache, uint8_t* v_cache, const float* k_scale,
+                                                const float* v_scale, const int32_t* block_tables,
+                                                const int32_t* context_lens, int batch, int num_q_heads,
+                                                int num_kv_heads, int head_dim, int block_size,
+                                                int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                                float scale, void* out, pkv_dtype q_dtype, int partition_tokens,
+                                                int64_t* slot_mapping_out, void* workspace, size_t workspace_bytes,
+                                                int32_t* err_flag, void* stream) {
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  return decode_common(true, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       max_context_len, scale, out, q_dtype, partition_tokens, workspace, workspace_bytes, err_flag,
+                       stream, k_new, v_new, slot_mapping_out);
+}
+
 extern "C" pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void* h_v_new,
                                            const int32_t* h_block_tables, const int32_t* h_context_lens,
                                            void* h_out, void* d_q, void* d_k_new, void* d_v_new,
@@ -268,16 +304,11 @@ extern "C" pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new,
                                   cudaMemcpyHostToDevice, s),
                   "cudaMemcpyAsync lens"))
     return PKV_ERR_CUDA;
-  pkv_status st = pkv_slot_mapping(d_block_tables, max_blocks_per_seq, num_blocks, nullptr, d_context_lens, -1,
-                                   batch, block_size, d_slots, err_flag, stream);
-  if (st != PKV_OK) return st;
-  st = pkv_kv_append(d_k_new, d_v_new, d_slots, batch, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                     block_size, dtype, err_flag, stream);
-  if (st != PKV_OK) return st;
-  st = pkv_paged_decode_attention(d_q, k_cache, v_cache, d_block_tables, d_context_lens, batch, num_q_heads,
-                                  num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
-                                  max_context_len, scale, d_out, dtype, partition_tokens, workspace,
-                                  workspace_bytes, err_flag, stream);
+  const pkv_status st = pkv_paged_decode_step(d_q, d_k_new, d_v_new, k_cache, v_cache, d_block_tables,
+                                              d_context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                              max_blocks_per_seq, num_blocks, max_context_len, scale, d_out, dtype,
+                                              partition_tokens, d_slots, workspace, workspace_bytes, err_flag,
+                                              stream);
   if (st != PKV_OK) return st;
   if (cuda_failed(cudaMemcpyAsync(h_out, d_out, qo_bytes, cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync out"))
     return PKV_ERR_CUDA;

@@ -70,13 +70,6 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
     k_cache[dst] = k_new[i];
 }
 
-// two floats -> two E4M3 codes, round to nearest even, saturate to +-448
-__device__ __forceinline__ uint16_t to_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // One thread quantises 8 elements (16 input bytes -> 8 code bytes).
 template <typename IN>
 __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
@@ -101,18 +94,9 @@ __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint
     return;
   }
   const float scale = is_v ? v_scale[h] : k_scale[h];
-  float x[8];
-  load8(is_v ? &v_new[i] : &k_new[i], x, IN{});
-  uint32_t w[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    // IEEE division (round to nearest even), not a reciprocal multiply
-    const float lo = __fdiv_rn(x[2 * e], scale), hi = __fdiv_rn(x[2 * e + 1], scale);
-    w[e] = to_e4m3x2(lo, hi);
-  }
+  const uint2 packed = quant8_e4m3(is_v ? &v_new[i] : &k_new[i], scale, IN{});
   const int64_t blk = s / kBlockSize, off = s % kBlockSize;
   const int64_t dst = ((blk * n_heads + h) * kBlockSize + off) * chunks_per_row + c;
-  const uint2 packed = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
   if (is_v)
     v_cache[dst] = packed;
   else

@@ -44,6 +44,12 @@
 //    16-bit type, transposed in registers (movmatrix) into the B operand of
 //    p.V, which accumulates O^T[head_dim x heads] in fp32 with V^T read by
 //    ldmatrix.trans.  The normaliser l sums the same rounded p.
+//
+// Fused step (k_new != null).  The same launch also appends each sequence's
+// new K/V row at position ctx - 1: thread blocks share the global writes in
+// their prologue (slots from the block table), and the consumer of the last
+// block of every (sequence, KV head) overwrites that row of its staged block
+// with the new row, so no block of the grid depends on another's write.
 #pragma once
 
 #include <cuda.h>
@@ -66,6 +72,9 @@ struct DecodeParams {
   const int32_t* block_tables;   // [B, max_blocks_per_seq]
   const int32_t* context_lens;   // [B]
   void* out;                     // [B, Hq, D] 16-bit
+  const void* k_new;             // fused step: [B, Hkv, D] rows appended at position ctx - 1 (else null)
+  const void* v_new;
+  int64_t* slots_out;            // fused step: [B] slots of the appended rows (nullable)
   int32_t* ws_cum;               // [B + 1] block-count prefix written for the combine
   float* ws_ml;                  // [slots, G, 2]
   float* ws_o;                   // [slots, G, D]
@@ -243,6 +252,40 @@ __device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int row, int chunk) 
 }
 
 // ---------------------------------------------------------------------------
+// fused step: write the new token's K and V rows over row r of a staged block
+// (swizzled [16 x 128 B] sub-tiles for the tensor-core layout, linear rows
+// otherwise).  One lane per 16-byte chunk of a cache row; E4M3 rows are
+// quantised exactly as the append kernel does.
+// ---------------------------------------------------------------------------
+// (out of line: it runs once per (sequence, KV head) and must not raise the
+// register allocation of the consumer loop)
+template <typename NT, int D, int ESZ, bool SWZ>
+__device__ __noinline__ void patch_new_row(uint32_t kslab, uint32_t vslab, int r, const void* k_row,
+                                              const void* v_row, float kscale, float vscale, int lane) {
+  constexpr int kChunks = D * ESZ / 16;    // 16-byte chunks per cache row
+  if (lane < 2 * kChunks) {
+    const bool is_v = lane >= kChunks;
+    const int c = is_v ? lane - kChunks : lane;
+    const uint32_t slab = is_v ? vslab : kslab;
+    const uint32_t addr = SWZ ? swz_addr(slab, r, c) : slab + r * D * ESZ + c * 16;
+    const unsigned char* src = static_cast<const unsigned char*>(is_v ? v_row : k_row);
+    uint4 v;
+    if constexpr (ESZ == 2) {
+      v = *reinterpret_cast<const uint4*>(src + c * 16);
+    } else {
+      const uint2 lo = quant8_e4m3(src + c * 32, is_v ? vscale : kscale, NT{});
+      const uint2 hi = quant8_e4m3(src + c * 32 + 16, is_v ? vscale : kscale, NT{});
+      v = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+    // order these generic-proxy writes before the stage's next TMA refill
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
 // the decode kernel
 // ---------------------------------------------------------------------------
 template <typename QT, typename KV, int D, int G, int NW, bool MMA>
@@ -322,6 +365,49 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
     for (int b = tid; b <= p.batch; b += blockDim.x) p.ws_cum[b] = cum[b];
 
   const int64_t R = p.part_blocks ? (W + p.part_blocks - 1) / p.part_blocks : gridDim.x;
+
+  // ---- 2. fused step: append the new rows (position ctx - 1) --------------
+  // The slot is computed from the block table here.  No thread block of this
+  // grid reads that slot from the cache: the consumer that processes the
+  // last block of (b, g) patches the row in shared memory instead (below).
+  using NT = std::conditional_t<T::kEsz == 1, QT, KV>;   // element type of the new rows
+  if (p.k_new != nullptr) {
+    constexpr int kChunks = D / 8;                           // 8 input elements per chunk
+    const int64_t total = 2ll * p.batch * Hkv * kChunks;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      int64_t x = idx;
+      const int c = static_cast<int>(x % kChunks);
+      x /= kChunks;
+      const int g = static_cast<int>(x % Hkv);
+      x /= Hkv;
+      const int b = static_cast<int>(x % p.batch);
+      const bool is_v = x >= p.batch;
+      const bool reports = !is_v && g == 0 && c == 0 && p.slots_out != nullptr;   // one thread per sequence
+      const int n = ntok[b];
+      if (n == 0) {
+        if (reports) p.slots_out[b] = -1;   // nothing appended (as the slot mapping reports padding)
+        continue;
+      }
+      const int pos = n - 1;
+      const int32_t blk = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + pos / kBlockSize];
+      if (blk < 0 || blk >= p.num_blocks) {
+        record_error(p.err, PKV_ERR_OOB);
+        if (reports) p.slots_out[b] = -1;
+        continue;
+      }
+      const int64_t row = (static_cast<int64_t>(blk) * Hkv + g) * kBlockSize + pos % kBlockSize;
+      if (reports) p.slots_out[b] = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
+      const unsigned char* src = static_cast<const unsigned char*>(is_v ? p.v_new : p.k_new) +
+                                 ((static_cast<int64_t>(b) * Hkv + g) * D + 8 * c) * 2;
+      unsigned char* dst =
+          static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache)) + (row * D + 8 * c) * T::kEsz;
+      if constexpr (T::kEsz == 2)
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+      else
+        *reinterpret_cast<uint2*>(dst) = quant8_e4m3(src, is_v ? scales[Hkv + g] : scales[g], NT{});
+    }
+  }
 
   if (warp == NW) {
     // ======================= producer warp ===============================
@@ -483,6 +569,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
     const float sc = p.qk_scale_log2 * scales[d.g];
     const int nseg = d.i1 - d.i0;
     const int first = static_cast<int>((warp + NW - (k_base % NW)) % NW);   // first local index for this warp
+    // fused step: local index of the block holding the new token (-1: none here)
+    const int patch_ii = (p.k_new != nullptr && d.i1 == d.nblk && d.n_tokens > 0) ? d.nblk - 1 - d.i0 : -1;
     float* mw = merge + warp * G * (D + 2);        // [G][D] o, then [G] m, [G] l
 
     if constexpr (MMA) {
@@ -535,6 +623,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
         const int n_valid = stage_ok[s] ? min(kBlockSize, d.n_tokens - i * kBlockSize) : 0;
         const uint32_t kslab = smem_u32(ring + static_cast<size_t>(s) * T::kStage);
         const uint32_t vslab = kslab + T::kSlab;
+        if (ii == patch_ii && n_valid > 0) {
+          const int64_t nr = (static_cast<int64_t>(d.b) * Hkv + d.g) * D * 2;
+          patch_new_row<NT, D, T::kEsz, true>(kslab, vslab, (d.n_tokens - 1) % kBlockSize,
+                                              static_cast<const unsigned char*>(p.k_new) + nr,
+                                              static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
+                                              scales[Hkv + d.g], lane);
+        }
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (kFp8) {
 #pragma unroll
@@ -668,6 +763,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
         const int n_valid = stage_ok[s] ? min(kBlockSize, d.n_tokens - i * kBlockSize) : 0;
         const unsigned char* kslab = ring + static_cast<size_t>(s) * T::kStage;
         const unsigned char* vslab = kslab + T::kSlab;
+        if (ii == patch_ii && n_valid > 0) {
+          const int64_t nr = (static_cast<int64_t>(d.b) * Hkv + d.g) * D * 2;
+          patch_new_row<NT, D, T::kEsz, false>(smem_u32(kslab), smem_u32(vslab), (d.n_tokens - 1) % kBlockSize,
+                                               static_cast<const unsigned char*>(p.k_new) + nr,
+                                               static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
+                                               scales[Hkv + d.g], lane);
+        }
 
         // ---- scores: partial dot products over this lane's 8 elements ----
         float part[T::kNV];

@@ -201,6 +201,26 @@ __device__ __forceinline__ void load8(const void* p, float* f, E4M3) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+// two floats -> two E4M3 codes (lo in the low byte), round to nearest even,
+// magnitudes above 448 clamp to 448
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 8 consecutive 16-bit elements -> 8 E4M3 codes of fl32(x) / scale (IEEE
+// division, not a reciprocal multiply), packed low byte first
+template <typename IN>
+__device__ __forceinline__ uint2 quant8_e4m3(const void* src, float scale, IN) {
+  float x[8];
+  load8(src, x, IN{});
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) w[e] = e4m3x2_from_f32(__fdiv_rn(x[2 * e], scale), __fdiv_rn(x[2 * e + 1], scale));
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
 // fp32 -> output element, round to nearest even
 __device__ __forceinline__ __half to_out(float x, F16) { return __float2half_rn(x); }
 __device__ __forceinline__ __nv_bfloat16 to_out(float x, BF16) { return __float2bfloat16_rn(x); }
