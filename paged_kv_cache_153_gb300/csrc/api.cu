@@ -69,7 +69,12 @@ int env_int(const char* name, int fallback) {
   return std::atoi(v);
 }
 
-constexpr int kMaxCtasPerSm = 4;
+constexpr int kMaxCtasPerSm = 4;   // partial slots are sized for this many blocks per SM
+// Cost of one (sequence, KV head) in the balanced split, in quarter blocks:
+// the per-segment work (query load, cross-warp merge, output or partial
+// write) and the consumer warps left idle by short segments.  Measured best
+// on GB300 at 24 (6 blocks' worth of streaming) for mixed context lengths.
+constexpr int kUnitCost = 24;
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -86,8 +91,9 @@ struct WsLayout {
   int64_t slots, ranges_cap;
 };
 
-// Workspace: [B + 1] int32 block-count prefix | [slots, G, 2] fp32 (m, l) |
-// [slots, G, D] fp32 o.  Two partial slots per range of the split.
+// Workspace: [2 (B + 1)] int32 block-count and non-empty-sequence prefixes |
+// [slots, G, 2] fp32 (m, l) | [slots, G, D] fp32 o.  Two partial slots per
+// range of the split.
 bool ws_layout(int batch, int n_kv_heads, int group, int head_dim, int max_blocks_per_seq, int max_context_len,
                int partition_tokens, int num_sms, WsLayout* w) {
   if (batch < 0 || n_kv_heads <= 0 || group <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
@@ -104,7 +110,7 @@ bool ws_layout(int batch, int n_kv_heads, int group, int head_dim, int max_block
   w->ranges_cap = ranges;
   w->slots = 2 * ranges;
   w->cum_off = 0;
-  w->ml_off = round256(sizeof(int32_t) * (static_cast<size_t>(batch) + 1));
+  w->ml_off = round256(sizeof(int32_t) * 2 * (static_cast<size_t>(batch) + 1));
   w->o_off = w->ml_off + round256(sizeof(float) * 2 * group * static_cast<size_t>(w->slots));
   w->total = w->o_off + round256(sizeof(float) * static_cast<size_t>(head_dim) * group * w->slots);
   return true;
@@ -172,12 +178,13 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_nblk = (max_context_len + kBlockSize - 1) / kBlockSize;
   p.part_blocks = partition_tokens / kBlockSize;
+  p.unit_cost = std::max(0, std::min(1 << 16, env_int("PKV_UNIT_COST", kUnitCost)));
   p.slot_capacity = static_cast<int>(w.slots);
   p.qk_scale_log2 = scale * kLog2e;
 
   LaunchInfo li{};
   li.num_sms = num_sms;
-  li.max_ctas_per_sm = std::max(1, std::min(kMaxCtasPerSm, env_int("PKV_CTAS_PER_SM", kMaxCtasPerSm)));
+  li.max_ctas_per_sm = std::max(0, std::min(kMaxCtasPerSm, env_int("PKV_CTAS_PER_SM", 0)));
   li.stages = env_int("PKV_STAGES", 0);
   li.part_ranges_cap = w.ranges_cap;
   return launch(p, li, static_cast<cudaStream_t>(stream));

@@ -75,7 +75,7 @@ struct DecodeParams {
   const void* k_new;             // fused step: [B, Hkv, D] rows appended at position ctx - 1 (else null)
   const void* v_new;
   int64_t* slots_out;            // fused step: [B] slots of the appended rows (nullable)
-  int32_t* ws_cum;               // [B + 1] block-count prefix written for the combine
+  int32_t* ws_cum;               // [2 (B + 1)]: block-count prefix, then non-empty-sequence prefix (for the combine)
   float* ws_ml;                  // [slots, G, 2]
   float* ws_o;                   // [slots, G, D]
   int32_t* err;
@@ -86,6 +86,7 @@ struct DecodeParams {
   int max_blocks_per_seq;
   int max_nblk;                  // ceil(max_context_len / 16)
   int part_blocks;               // 0 = balanced ranges
+  int unit_cost;                 // balanced ranges: cost of a (sequence, KV head), in quarter blocks
   int slot_capacity;             // number of partial slots in the workspace
   int stages;                    // multiple of the consumer warp count
   float qk_scale_log2;           // softmax scale * log2(e)
@@ -97,6 +98,14 @@ struct SegDesc {
   int nblk;                      // blocks of (b, g)
   int slot;                      // -1 = write out directly, -2 = dropped, else partial slot
   int end;                       // 1 = no more segments
+};
+
+// producer-side view of a segment
+struct ProdSeg {
+  int b, g, i0, i1, nb;
+  int slot;                      // as SegDesc::slot
+  int64_t r;                     // its range
+  int64_t f_end, f_hi;           // flat end of the segment and of its range
 };
 
 // number of blocks of sequence b after clamping to the table and the bound
@@ -117,6 +126,38 @@ __device__ __forceinline__ int seq_blocks(const DecodeParams& p, int ctx, int32_
 // flat index of range boundary r
 __device__ __forceinline__ int64_t range_start(int64_t r, int64_t W, int64_t R, int part_blocks) {
   return part_blocks ? min(r * part_blocks, W) : (r * W) / R;
+}
+
+// Balanced ranges split a cost axis, not the block axis: every block costs
+// kBlockCost and every non-empty (sequence, KV head) adds unit_cost ahead of
+// its first block (the per-segment work: query load, merge, output), so
+// ranges that hold many short sequences get fewer blocks.  Block i of
+// (b, g) sits at cost
+//   pos = C(b) + g (kBlockCost nb + A) + A + kBlockCost i,
+//   C(b) = Hkv (kBlockCost cum[b] + A ne[b])
+// (cum: block prefix, ne: non-empty-sequence prefix, A = unit_cost), and
+// range r of R owns the blocks with floor(r V / R) <= pos < floor((r+1) V / R).
+constexpr int kBlockCost = 4;
+
+__device__ __forceinline__ int64_t seq_cost(const int* cum, const int* ne, int b, int Hkv, int A) {
+  return static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * cum[b] + static_cast<int64_t>(A) * ne[b]);
+}
+
+// number of blocks whose cost position is below v (0 <= v <= V)
+__device__ __forceinline__ int64_t blocks_before_cost(int64_t v, const int* cum, const int* ne, int batch, int Hkv,
+                                                      int A) {
+  if (v >= seq_cost(cum, ne, batch, Hkv, A)) return static_cast<int64_t>(Hkv) * cum[batch];
+  int lo = 0, hi = batch - 1;   // largest b with C(b) <= v: a non-empty sequence
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (seq_cost(cum, ne, mid, Hkv, A) <= v) lo = mid; else hi = mid - 1;
+  }
+  const int nb = cum[lo + 1] - cum[lo];
+  const int64_t unit = static_cast<int64_t>(kBlockCost) * nb + A;
+  const int64_t rem = v - seq_cost(cum, ne, lo, Hkv, A);
+  const int64_t g = rem / unit, w = rem % unit;
+  const int64_t cnt = (w <= A) ? 0 : min(static_cast<int64_t>(nb), (w - A + kBlockCost - 1) / kBlockCost);
+  return static_cast<int64_t>(Hkv) * cum[lo] + g * nb + cnt;
 }
 
 template <int D, int G, int NW, typename KV, bool MMA>
@@ -156,7 +197,7 @@ struct DecodeTraits {
   }
   // + 1024 bytes so that the base can be rounded up to a 1024-byte boundary
   static __host__ __device__ size_t smem_bytes(int stages, int batch, int n_kv_heads) {
-    return 1024 + cum_off(stages, n_kv_heads) + 4 * (2 * static_cast<size_t>(batch) + 2);
+    return 1024 + cum_off(stages, n_kv_heads) + 4 * (3 * static_cast<size_t>(batch) + 3);
   }
 };
 
@@ -289,7 +330,7 @@ __device__ __noinline__ void patch_new_row(uint32_t kslab, uint32_t vslab, int r
 // the decode kernel
 // ---------------------------------------------------------------------------
 template <typename QT, typename KV, int D, int G, int NW, bool MMA>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   using T = DecodeTraits<D, G, NW, KV, MMA>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -309,8 +350,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc));
   int* warp_tot = reinterpret_cast<int*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc) + 16);
   float* scales = reinterpret_cast<float*>(smem + T::scales_off(S));
-  int* cum = reinterpret_cast<int*>(smem + T::cum_off(S, p.n_kv_heads));   // [B + 1]
+  int* cum = reinterpret_cast<int*>(smem + T::cum_off(S, p.n_kv_heads));   // [B + 1] block prefix
   int* ntok = cum + p.batch + 1;                                             // [B]
+  int* ne = ntok + p.batch;                                                  // [B + 1] non-empty prefix
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads;
@@ -322,7 +364,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
     scales[h] = p.k_scale ? p.k_scale[h] : 1.0f;
     scales[Hkv + h] = p.v_scale ? p.v_scale[h] : 1.0f;
   }
-  int carry = 0;
+  static_assert(NW + 1 <= 16, "warp totals: 16 slots per scanned quantity");
+  int carry = 0, carry_ne = 0;
   for (int base = 0; base < p.batch; base += blockDim.x) {
     const int b = base + tid;
     int nb = 0;
@@ -331,24 +374,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
       nb = seq_blocks(p, ctx, p.err);
       ntok[b] = min(max(ctx, 0), nb * kBlockSize);
     }
-    int x = nb;   // inclusive block-wide scan
+    int x = nb, y = nb > 0 ? 1 : 0;   // inclusive block-wide scans: blocks, non-empty sequences
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const int xu = __shfl_up_sync(0xffffffffu, x, o);
+      const int yu = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) {
+        x += xu;
+        y += yu;
+      }
     }
-    if (lane == 31) warp_tot[warp] = x;
+    if (lane == 31) {
+      warp_tot[warp] = x;
+      warp_tot[16 + warp] = y;
+    }
     __syncthreads();
-    int before = 0;
-    for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
-    if (b < p.batch) cum[b + 1] = carry + before + x;
-    int tot = 0;
-    for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) tot += warp_tot[w2];
-    carry += tot;
+    int before = 0, before_ne = 0;
+    for (int w2 = 0; w2 < warp; ++w2) {
+      before += warp_tot[w2];
+      before_ne += warp_tot[16 + w2];
+    }
+    if (b < p.batch) {
+      cum[b + 1] = carry + before + x;
+      ne[b + 1] = carry_ne + before_ne + y;
+    }
+    for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) {
+      carry += warp_tot[w2];
+      carry_ne += warp_tot[16 + w2];
+    }
     __syncthreads();
   }
   if (tid == 0) {
     cum[0] = 0;
+    ne[0] = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -362,20 +420,26 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
   __syncthreads();
   const int64_t W = static_cast<int64_t>(Hkv) * cum[p.batch];
   if (blockIdx.x == 0 && p.ws_cum != nullptr)
-    for (int b = tid; b <= p.batch; b += blockDim.x) p.ws_cum[b] = cum[b];
+    for (int b = tid; b <= p.batch; b += blockDim.x) {
+      p.ws_cum[b] = cum[b];
+      p.ws_cum[p.batch + 1 + b] = ne[b];
+    }
 
   const int64_t R = p.part_blocks ? (W + p.part_blocks - 1) / p.part_blocks : gridDim.x;
+  const int A = p.unit_cost;
+  const int64_t V = seq_cost(cum, ne, p.batch, Hkv, A);   // balanced mode: total cost
 
   // ---- 2. fused step: append the new rows (position ctx - 1) --------------
   // The slot is computed from the block table here.  No thread block of this
   // grid reads that slot from the cache: the consumer that processes the
   // last block of (b, g) patches the row in shared memory instead (below).
+  // The consumer warps do the writes; the producer starts streaming at once.
   using NT = std::conditional_t<T::kEsz == 1, QT, KV>;   // element type of the new rows
-  if (p.k_new != nullptr) {
+  if (p.k_new != nullptr && warp < NW) {
     constexpr int kChunks = D / 8;                           // 8 input elements per chunk
     const int64_t total = 2ll * p.batch * Hkv * kChunks;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * (NW * 32) + tid; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * (NW * 32)) {
       int64_t x = idx;
       const int c = static_cast<int>(x % kChunks);
       x /= kChunks;
@@ -384,6 +448,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
       const int b = static_cast<int>(x % p.batch);
       const bool is_v = x >= p.batch;
       const bool reports = !is_v && g == 0 && c == 0 && p.slots_out != nullptr;   // one thread per sequence
+      // the new row's chunk is loaded before the table entry, so both loads are in flight together
+      const unsigned char* src = static_cast<const unsigned char*>(is_v ? p.v_new : p.k_new) +
+                                 ((static_cast<int64_t>(b) * Hkv + g) * D + 8 * c) * 2;
+      const uint4 raw = *reinterpret_cast<const uint4*>(src);
       const int n = ntok[b];
       if (n == 0) {
         if (reports) p.slots_out[b] = -1;   // nothing appended (as the slot mapping reports padding)
@@ -398,14 +466,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
       }
       const int64_t row = (static_cast<int64_t>(blk) * Hkv + g) * kBlockSize + pos % kBlockSize;
       if (reports) p.slots_out[b] = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
-      const unsigned char* src = static_cast<const unsigned char*>(is_v ? p.v_new : p.k_new) +
-                                 ((static_cast<int64_t>(b) * Hkv + g) * D + 8 * c) * 2;
       unsigned char* dst =
           static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache)) + (row * D + 8 * c) * T::kEsz;
       if constexpr (T::kEsz == 2)
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        *reinterpret_cast<uint4*>(dst) = raw;
       else
-        *reinterpret_cast<uint2*>(dst) = quant8_e4m3(src, is_v ? scales[Hkv + g] : scales[g], NT{});
+        *reinterpret_cast<uint2*>(dst) = quant8_e4m3(&raw, is_v ? scales[Hkv + g] : scales[g], NT{});
     }
   }
 
@@ -420,105 +486,146 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const __
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
     }
     uint32_t k = 0, j = 0;
-    for (int64_t r = blockIdx.x; r < R && !*abort_flag; r += (p.part_blocks ? gridDim.x : R)) {
-      const int64_t f_lo = range_start(r, W, R, p.part_blocks);
-      const int64_t f_hi = range_start(r + 1, W, R, p.part_blocks);
-      int64_t f = f_lo;
-      while (f < f_hi && !*abort_flag) {
-        // locate the sequence: largest b with Hkv * cum[b] <= f
-        int lo = 0, hi = p.batch - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (static_cast<int64_t>(Hkv) * cum[mid] <= f) lo = mid; else hi = mid - 1;
+    // Segments in order: the ranges of this thread block (one in balanced
+    // mode; blockIdx.x, + gridDim.x, ... in partition mode), each cut at
+    // (sequence, KV head) boundaries.
+    const int64_t r_step = p.part_blocks ? gridDim.x : R;
+    auto bounds = [&](int64_t r, int64_t& lo, int64_t& hi) {
+      if (p.part_blocks) {
+        lo = range_start(r, W, R, p.part_blocks);
+        hi = range_start(r + 1, W, R, p.part_blocks);
+      } else {
+        lo = blocks_before_cost((r * V) / R, cum, ne, p.batch, Hkv, A);
+        hi = blocks_before_cost(((r + 1) * V) / R, cum, ne, p.batch, Hkv, A);
+      }
+    };
+    // the segment that starts at block f of range r = [f_lo, f_hi)
+    auto locate = [&](int64_t r, int64_t f, int64_t f_lo, int64_t f_hi, ProdSeg& sg) {
+      int lo = 0, hi = p.batch - 1;   // largest b with Hkv * cum[b] <= f
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(Hkv) * cum[mid] <= f) lo = mid; else hi = mid - 1;
+      }
+      sg.b = lo;
+      sg.nb = cum[lo + 1] - cum[lo];
+      const int64_t rem = f - static_cast<int64_t>(Hkv) * cum[lo];
+      sg.g = static_cast<int>(rem / sg.nb);
+      sg.i0 = static_cast<int>(rem % sg.nb);
+      sg.f_end = min(f_hi, f + (sg.nb - sg.i0));
+      sg.i1 = sg.i0 + static_cast<int>(sg.f_end - f);
+      sg.r = r;
+      sg.f_hi = f_hi;
+      sg.slot = -1;
+      if (!(sg.i0 == 0 && sg.i1 == sg.nb)) {
+        const int64_t sl = (f == f_lo) ? 2 * r : 2 * r + 1;
+        sg.slot = (sl < p.slot_capacity) ? static_cast<int>(sl) : -2;   // -2: computed but not stored
+      }
+    };
+    // the first segment of the first non-empty range from r on
+    auto first_from = [&](int64_t r, ProdSeg& sg) -> bool {
+      for (; r < R; r += r_step) {
+        int64_t lo, hi;
+        bounds(r, lo, hi);
+        if (lo < hi) {
+          locate(r, lo, lo, hi, sg);
+          return true;
         }
-        const int b = lo;
-        const int nb = cum[b + 1] - cum[b];
-        const int64_t rem = f - static_cast<int64_t>(Hkv) * cum[b];
-        const int g = static_cast<int>(rem / nb);
-        const int i0 = static_cast<int>(rem % nb);
-        const int64_t f_end = min(f_hi, f + (nb - i0));
-        const int i1 = i0 + static_cast<int>(f_end - f);
-        int slot = -1;
-        if (!(i0 == 0 && i1 == nb)) {
-          const int64_t sl = (f == f_lo) ? 2 * r : 2 * r + 1;
-          if (sl >= p.slot_capacity) {
-            record_error(p.err, PKV_ERR_WORKSPACE);
-            slot = -2;                       // computed but not stored
-          } else {
-            slot = static_cast<int>(sl);
-          }
+      }
+      return false;
+    };
+    auto next_of = [&](const ProdSeg& cur, ProdSeg& sg) -> bool {
+      if (cur.f_end < cur.f_hi) {
+        locate(cur.r, cur.f_end, -1, cur.f_hi, sg);
+        return true;
+      }
+      return first_from(cur.r + r_step, sg);
+    };
+    // table entry i0 + w + lane of a segment (0 past its end)
+    auto table_at = [&](const ProdSeg& sg, int w) -> int {
+      return (sg.i0 + w + lane < sg.i1)
+                 ? p.block_tables[static_cast<int64_t>(sg.b) * p.max_blocks_per_seq + sg.i0 + w + lane]
+                 : 0;
+    };
+    ProdSeg cur;
+    bool have = first_from(blockIdx.x, cur);
+    int ids = have ? table_at(cur, 0) : 0;
+    while (have && !*abort_flag) {
+      if (cur.slot == -2) record_error(p.err, PKV_ERR_WORKSPACE);
+      // publish the segment descriptor and its query rows
+      const int qs = j & 1;
+      if (lane == 0) {
+        if (j >= 2 && !*abort_flag && !mbar_wait(&qempty_bar[qs], ((j >> 1) - 1) & 1, p.err)) *abort_flag = 1;
+        SegDesc d;
+        d.b = cur.b; d.g = cur.g; d.i0 = cur.i0; d.i1 = cur.i1; d.n_tokens = ntok[cur.b]; d.nblk = cur.nb;
+        d.slot = cur.slot;
+        d.end = *abort_flag ? 1 : 0;
+        seg[qs] = d;
+        if (!*abort_flag) {
+          mbar_arrive_expect_tx(&qfull_bar[qs], T::kQBytes);
+          bulk_g2s(q_ring + qs * T::kQBytes,
+                   qbase + (static_cast<int64_t>(cur.b) * p.n_q_heads + static_cast<int64_t>(cur.g) * G) * D * 2,
+                   T::kQBytes, &qfull_bar[qs], pol_stream);
+        } else {
+          mbar_arrive(&qfull_bar[qs]);
         }
-        // publish the segment descriptor and its query rows
-        const int qs = j & 1;
-        if (lane == 0) {
-          if (j >= 2 && !*abort_flag && !mbar_wait(&qempty_bar[qs], ((j >> 1) - 1) & 1, p.err)) *abort_flag = 1;
-          SegDesc d;
-          d.b = b; d.g = g; d.i0 = i0; d.i1 = i1; d.n_tokens = ntok[b]; d.nblk = nb; d.slot = slot;
-          d.end = *abort_flag ? 1 : 0;
-          seg[qs] = d;
-          if (!*abort_flag) {
-            mbar_arrive_expect_tx(&qfull_bar[qs], T::kQBytes);
-            bulk_g2s(q_ring + qs * T::kQBytes,
-                     qbase + (static_cast<int64_t>(b) * p.n_q_heads + static_cast<int64_t>(g) * G) * D * 2,
-                     T::kQBytes, &qfull_bar[qs], pol_stream);
-          } else {
-            mbar_arrive(&qfull_bar[qs]);
-          }
-        }
-        __syncwarp();
-        ++j;
-        // Stream the segment's K/V slabs.  Lane j of the producer warp owns
-        // block j of each 32-block window of the table (its table entry is
-        // loaded by that lane, one window ahead).  The window is issued in
-        // sub-batches of min(S, 32) blocks: the blocks of a sub-batch occupy
-        // distinct stages, so their lanes wait and issue in parallel; the
-        // __syncwarp between sub-batches keeps each stage's uses in order.
-        const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-        const int sub = S < 32 ? S : 32;
-        int ids = (i0 + lane < i1) ? row[i0 + lane] : 0;
-        for (int ib = i0; ib < i1; ib += 32) {
-          const int nxt = (ib + 32 + lane < i1) ? row[ib + 32 + lane] : 0;   // prefetch the next window
-          const int cnt = min(32, i1 - ib);
-          for (int sb = 0; sb < cnt; sb += sub) {
-            if (lane >= sb && lane < min(sb + sub, cnt) && !*abort_flag) {
-              const uint32_t kk = k + lane;                        // CTA-local block counter
-              const uint32_t jw = kk / NW;                         // index in its warp's ring
-              const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
-              const uint32_t use = jw / SPW;
-              bool ok = ids >= 0 && ids < p.num_blocks;
-              if (use >= 1 && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.err)) {
-                *abort_flag = 1;
-                ok = false;
-              }
-              stage_ok[s] = ok ? 1 : 0;
-              unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
-              if (ok) {
-                mbar_arrive_expect_tx(&full_bar[s], T::kStage);
-                if constexpr (MMA) {
-                  const int y = (ids * Hkv + g) * kBlockSize;
+      }
+      __syncwarp();
+      ++j;
+      ProdSeg nxt;
+      const bool have_nxt = next_of(cur, nxt);
+      // Stream the segment's K/V slabs.  Lane j of the producer warp owns
+      // block j of each 32-block window of the table (its table entry is
+      // loaded by that lane one window ahead; the last window of a segment
+      // loads the first window of the next segment).  The window is issued
+      // in sub-batches of min(S, 32) blocks: the blocks of a sub-batch
+      // occupy distinct stages, so their lanes wait and issue in parallel;
+      // the __syncwarp between sub-batches keeps each stage's uses in order.
+      const int g = cur.g;
+      const int sub = S < 32 ? S : 32;
+      const int nseg = cur.i1 - cur.i0;
+      for (int w0 = 0; w0 < nseg; w0 += 32) {
+        const int nxt_ids = (w0 + 32 < nseg) ? table_at(cur, w0 + 32) : (have_nxt ? table_at(nxt, 0) : 0);
+        const int cnt = min(32, nseg - w0);
+        for (int sb = 0; sb < cnt; sb += sub) {
+          if (lane >= sb && lane < min(sb + sub, cnt) && !*abort_flag) {
+            const uint32_t kk = k + lane;                        // CTA-local block counter
+            const uint32_t jw = kk / NW;                         // index in its warp's ring
+            const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
+            const uint32_t use = jw / SPW;
+            bool ok = ids >= 0 && ids < p.num_blocks;
+            if (use >= 1 && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.err)) {
+              *abort_flag = 1;
+              ok = false;
+            }
+            stage_ok[s] = ok ? 1 : 0;
+            unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
+            if (ok) {
+              mbar_arrive_expect_tx(&full_bar[s], T::kStage);
+              if constexpr (MMA) {
+                const int y = (ids * Hkv + g) * kBlockSize;
 #pragma unroll
-                  for (int t = 0; t < T::kSubTiles; ++t) {
-                    tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
-                    tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
-                                pol_stream);
-                  }
-                } else {
-                  const int64_t slab = (static_cast<int64_t>(ids) * Hkv + g) * T::kSlab;
-                  bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
-                  bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
+                for (int t = 0; t < T::kSubTiles; ++t) {
+                  tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
+                  tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
+                              pol_stream);
                 }
               } else {
-                if (!*abort_flag) record_error(p.err, PKV_ERR_OOB);
-                mbar_arrive(&full_bar[s]);
+                const int64_t slab = (static_cast<int64_t>(ids) * Hkv + g) * T::kSlab;
+                bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
+                bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
               }
+            } else {
+              if (!*abort_flag) record_error(p.err, PKV_ERR_OOB);
+              mbar_arrive(&full_bar[s]);
             }
-            __syncwarp();
           }
-          k += cnt;
-          ids = nxt;
+          __syncwarp();
         }
-        f = f_end;
+        k += cnt;
+        ids = nxt_ids;
       }
+      cur = nxt;
+      have = have_nxt;
     }
     // end marker
     const int qs = j & 1;
@@ -962,17 +1069,41 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
     if (live_t && sub == 0) store4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int64_t W = static_cast<int64_t>(p.n_kv_heads) * p.ws_cum[p.batch];
-  const int64_t S0 = static_cast<int64_t>(p.n_kv_heads) * c0 + static_cast<int64_t>(g) * nb;
-  const int64_t E0 = S0 + nb;
+  const int Hkv = p.n_kv_heads;
+  const int64_t W = static_cast<int64_t>(Hkv) * p.ws_cum[p.batch];
+  const int64_t S0 = static_cast<int64_t>(Hkv) * c0 + static_cast<int64_t>(g) * nb;
   const int64_t R = p.part_blocks ? (W + p.part_blocks - 1) / p.part_blocks : grid_ranges;
-  auto range_of = [&](int64_t f) -> int64_t {
-    if (p.part_blocks) return f / p.part_blocks;
-    return ((f + 1) * R + W - 1) / W - 1;
-  };
-  const int64_t r0 = range_of(S0), r1 = range_of(E0 - 1);
+  // Balanced mode works on the cost axis (see blocks_before_cost): u0 is the
+  // cost where (b, g) starts, pos0 that of its first block; the block before
+  // S0, if any, is the last of the previous non-empty pair, at u0 - kBlockCost.
+  const int A = p.unit_cost;
+  const int64_t V = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * p.ws_cum[p.batch] +
+                                                 static_cast<int64_t>(A) * p.ws_cum[2 * p.batch + 1]);
+  const int64_t u0 = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * c0 +
+                                                  static_cast<int64_t>(A) * p.ws_cum[p.batch + 1 + b]) +
+                     static_cast<int64_t>(g) * (static_cast<int64_t>(kBlockCost) * nb + A);
+  const int64_t pos0 = u0 + A;
+  auto vr = [&](int64_t r) -> int64_t { return (r * V) / R; };   // start cost of range r
+  int64_t r0, r1;
+  bool first_is_head;
+  if (p.part_blocks) {
+    r0 = S0 / p.part_blocks;
+    r1 = (S0 + nb - 1) / p.part_blocks;
+    first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
+  } else {
+    r0 = ((pos0 + 1) * R + V - 1) / V - 1;   // largest r with vr(r) <= pos0
+    const int64_t posl = pos0 + static_cast<int64_t>(kBlockCost) * (nb - 1);
+    r1 = ((posl + 1) * R + V - 1) / V - 1;
+    first_is_head = (S0 == 0) || (vr(r0) > u0 - kBlockCost);
+  }
   if (r0 == r1) return;   // one segment: written by the decode kernel
-  const bool first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
+  // a range after r0 holds a block of (b, g) unless it is narrower than a block
+  auto has_piece = [&](int64_t r) -> bool {
+    if (p.part_blocks) return range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
+    if (r == r0) return true;
+    const int64_t i = (vr(r) - pos0 + kBlockCost - 1) / kBlockCost;
+    return pos0 + static_cast<int64_t>(kBlockCost) * i < vr(r + 1);
+  };
   const int h = live_t ? (4 * t) / D : 0, e = live_t ? (4 * t) % D : 0;
   float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
   constexpr int kBatch = WIDE ? 4 : 8;   // partials whose loads are issued together, per lane
@@ -984,8 +1115,7 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
       const int64_t r = rb + static_cast<int64_t>(q) * kSplit;
       // ranges between r0 and r1 may be empty (fewer blocks than ranges):
       // they wrote nothing for this (b, g)
-      const bool live = live_t && r <= r1 &&
-                        range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
+      const bool live = live_t && r <= r1 && has_piece(r);
       const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
       ml[q] = live ? *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2) : make_float2(-INFINITY, 0.f);
       ov[q] = live ? *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e) : make_float4(0.f, 0.f, 0.f, 0.f);

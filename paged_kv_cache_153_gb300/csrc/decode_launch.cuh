@@ -13,7 +13,7 @@ namespace pkv {
 
 struct LaunchInfo {
   int num_sms;
-  int max_ctas_per_sm;     // cap on resident decode blocks per SM
+  int max_ctas_per_sm;     // resident decode blocks per SM (0 = the variant's default)
   int stages;              // 0 = fill the SM's shared memory; else a request (rounded to the warp count)
   int grid;                // out: decode grid used
   int64_t part_ranges_cap; // partition mode: max ranges the workspace holds
@@ -63,10 +63,12 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
                   "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  // resident blocks per SM: measured best on GB300 at 2 for the CUDA-core
-  // variant (8 consumer warps each) and at the register limit (3) for the
-  // tensor-core variant (4 consumer warps each)
-  occ = std::min(occ, std::min(li.max_ctas_per_sm, MMA ? 4 : 2));
+  // Resident blocks per SM (li.max_ctas_per_sm overrides), measured best on
+  // GB300: 2 for 16-bit caches, where a deeper stage ring per block beats more
+  // consumer warps; 3 for E4M3 through the tensor cores, whose per-block
+  // conversions want more consumer warps.
+  const int want = li.max_ctas_per_sm > 0 ? li.max_ctas_per_sm : ((MMA && Tr::kEsz == 1) ? 3 : 2);
+  occ = std::min(occ, want);
   int spw = 1;
   if (li.stages > 0) {
     spw = std::max(1, li.stages / NW);
@@ -87,7 +89,7 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
                   "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  occ = std::min(occ, std::min(li.max_ctas_per_sm, MMA ? 4 : 2));
+  occ = std::min(occ, want);
   int grid = li.num_sms * occ;
   if (p.part_blocks > 0 && li.part_ranges_cap < grid) grid = static_cast<int>(li.part_ranges_cap);
   // a small workload (upper bound on blocks known from max_context_len) needs
