@@ -323,15 +323,17 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         raise RuntimeError(f"device error {int(err.item())} during warm-up")
     log("warm-up done")
 
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    # The timed steps run back to back on one stream.  The roofline's kernel
+    # time is the same events' average per call: events recorded between
+    # calls would end each call's programmatic overlap with the next one and
+    # time a launch pattern the loop does not have.
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
         barrier()
         torch.cuda.synchronize(dev)
         t_start.record(stream)
-        for i in range(args.steps):
-            step(*ev_dec[i])
+        for _ in range(args.steps):
+            step()
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -339,8 +341,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     log(f"timed region done: {elapsed_ms / args.steps:.4f} ms per step")
     if int(err.item()) != 0:
         raise RuntimeError(f"device error {int(err.item())} in the timed region")
-    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    dec_avg_ms = elapsed_ms / args.steps   # this rank's calls, on the launching stream
     if dist is not None:
         elapsed_ms = max_over_ranks(elapsed_ms, dist, dev if dist.get_backend() == "nccl" else "cpu")
 
@@ -390,7 +391,8 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         "config": dict(describe(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-                     "kernel": "pkv_paged_decode_step call (decode kernel with slot mapping and append, then the combine kernel)",
+                     "kernel": "pkv_paged_decode_step call (decode kernel with slot mapping and append, then the combine kernel), "
+                               "average over the back-to-back calls of the timed region",
                      "algorithmic_bytes_per_launch": algo, "avg_launch_ms": dec_avg_ms,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "frac_of_8TBps": achieved / 8000.0},
@@ -402,13 +404,135 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     return res
 
 
+# ---------------------------------------------------------------------------
+# copy-on-write block copy (--workload cow)
+# ---------------------------------------------------------------------------
+COPY_METRIC = "copy-on-write block copy GB/s (K and V bytes read + written), 1 GPU"
+COPY_SHAPE = {"num_blocks": 32768, "n_pairs": 8192, "n_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
+
+
+def copy_config() -> dict:
+    c = COPY_SHAPE
+    block_bytes = c["n_kv_heads"] * 16 * c["head_dim"] * 2
+    return {"workload": f"cow: {c['n_pairs']} block copies per step (a fork storm) in a pool of {c['num_blocks']} "
+                        f"blocks of {c['n_kv_heads']} KV heads x 16 x {c['head_dim']} {c['dtype']}, K and V caches",
+            "block_bytes_per_cache": block_bytes, "l2": f"{4 * c['n_pairs'] * block_bytes / 1e9:.2f} GB moved "
+            "per step (larger than L2), no flush", **c}
+
+
+def oracle_copy_rate(budget_s: float) -> tuple[float, str]:
+    """The oracle's block copy on the host: GB/s over a bounded sample."""
+    from oracle import slots as osl
+    c = COPY_SHAPE
+    nb, n = 512, 128
+    rng = np.random.Generator(np.random.PCG64(77))
+    k = rng.integers(0, 2 ** 16, size=(nb, c["n_kv_heads"], 16, c["head_dim"]), dtype=np.uint16)
+    v = k.copy()
+    src, dst = wl.copy_pairs(nb, n, seed=78)
+    pairs = list(zip(src.tolist(), dst.tolist()))
+    moved, t0 = 0, time.perf_counter()
+    while True:
+        osl.copy_blocks(k, pairs)
+        osl.copy_blocks(v, pairs)
+        moved += 4 * n * k[0].nbytes
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return moved / el / 1e9, f"{n} block copies per pass in a {nb}-block pool, {el:.1f} s, one host thread"
+
+
+def copy_bytes_per_step() -> int:
+    c = COPY_SHAPE
+    return 4 * c["n_pairs"] * c["n_kv_heads"] * 16 * c["head_dim"] * 2
+
+
+def run_copy(args, rank: int, local_rank: int) -> dict | None:
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import paged_kv_cache_153_gb300 as pkv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    c = COPY_SHAPE
+    stream = torch.cuda.Stream(device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1200)
+    shape = (c["num_blocks"], c["n_kv_heads"], 16, c["head_dim"])
+    with torch.cuda.stream(stream):
+        k_cache = torch.randint(-2 ** 15, 2 ** 15, shape, dtype=torch.int16, device=dev, generator=gen).view(
+            torch.bfloat16)
+        v_cache = torch.randint(-2 ** 15, 2 ** 15, shape, dtype=torch.int16, device=dev, generator=gen).view(
+            torch.bfloat16)
+        src_np, dst_np = wl.copy_pairs(c["num_blocks"], c["n_pairs"], seed=1201)
+        src, dst = torch.from_numpy(src_np).to(dev), torch.from_numpy(dst_np).to(dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream.synchronize()
+    moved = 4 * c["n_pairs"] * k_cache[0].numel() * 2
+
+    def step():
+        pkv.pkv_copy_blocks(src, dst, k_cache, v_cache, err_flag=err, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step()
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())} in the timed region")
+    per_ms = elapsed_ms / args.steps
+    gbs = moved / (per_ms * 1e-3) / 1e9
+    # end to end: the step's pair list from pinned host memory, the error word read back
+    h_src, h_dst = torch.from_numpy(src_np).pin_memory(), torch.from_numpy(dst_np).pin_memory()
+    h_err = torch.zeros(1, dtype=torch.int32).pin_memory()
+    d_src, d_dst = torch.empty_like(src), torch.empty_like(dst)
+
+    def host_step():
+        d_src.copy_(h_src, non_blocking=True)
+        d_dst.copy_(h_dst, non_blocking=True)
+        pkv.pkv_copy_blocks(d_src, d_dst, k_cache, v_cache, err_flag=err, stream=stream)
+        h_err.copy_(err, non_blocking=True)
+        stream.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            host_step()
+        n_e2e = max(10, min(args.steps, 500))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        e2e_s = time.perf_counter() - t0
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    cfg = copy_config()
+    return {
+        "metric": COPY_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": ncu_traffic("cow"), "kernel": "copy_blocks_kernel (pkv_copy_blocks), average over "
+                     "the back-to-back calls of the timed region", "algorithmic_bytes_per_launch": moved,
+                     "avg_launch_ms": per_ms, "peak_kind": f"{peak_kind} HBM copy bandwidth"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "e2e": {"value": moved * n_e2e / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h_src.numel() * 4 + h_dst.numel() * 4), "d2h_bytes_per_step": 4,
+                "steps": n_e2e, "path": "pair lists from pinned host memory, pkv_copy_blocks, error word read back"},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES))
+    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -416,6 +540,30 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == "cow":
+        if args.impl == "reference":
+            if rank != 0:
+                return
+            rate, sample = oracle_copy_rate(budget_s=max(1.0, 0.02 * args.steps))
+            print(json.dumps({
+                "impl": "reference", "metric": COPY_METRIC, "value": rate, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": copy_bytes_per_step() / (rate * 1e9) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": copy_config(),
+                "cpu_baseline": {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+                "e2e": {"value": rate, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+            return
+        res = run_copy(args, rank, local_rank)
+        if res is not None:
+            if not args.no_cpu_baseline:
+                rate, sample = oracle_copy_rate(budget_s=10.0)
+                res["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                       "sample": sample}
+            print(json.dumps(res), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:

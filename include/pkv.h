@@ -280,6 +280,57 @@ int32_t pkv_pool_refcount(const pkv_pool* pool, int32_t block_id);   /* -1 for a
 /* Blocks needed for n tokens: ceil(n / block_size) ("Series 03 ...", 3.2). */
 int64_t pkv_blocks_needed(int64_t num_tokens, int block_size);
 
+/* ---------------------------------------------------------------------------
+ * Copy-on-write ("Series 03 ...", section 3.3: the branches of a beam search,
+ * or parallel samples, share the prefix blocks without copying; when a branch
+ * writes its first token of its own into a shared block, a new block is taken,
+ * the old contents are copied into it and the token is written there, while
+ * the other branches keep the old block).
+ *
+ * pkv_pool_cow: make block_id private before a write.  Reference count 1:
+ * *out_id = block_id, nothing changes.  Otherwise a fresh block is taken
+ * (reference count 1), block_id loses one reference and *out_id is the new
+ * id; the caller points its table at it and copies block_id into it
+ * (pkv_copy_blocks) before writing.  PKV_ERR_NO_BLOCKS (nothing changed) when
+ * the pool is empty, PKV_ERR_INVALID_ARG for an id that is not allocated.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_pool_cow(pkv_pool* pool, int32_t block_id, int32_t* out_id);
+
+/* Host side of one decode step over tables that may share blocks.  For each
+ * sequence b the step's token sits at position p = context_lens[b] - 1 (the
+ * length after the append; 0 means no token for b).  Entry i = p / block_size
+ * of row b of block_tables ([batch, max_blocks_per_seq], host memory):
+ *   - negative: the sequence grows into a new block; a fresh block is taken
+ *     and stored there;
+ *   - a shared block: pkv_pool_cow, the new id is stored and the pair
+ *     (old, new) is appended to src_blocks / dst_blocks (host arrays of
+ *     capacity batch);
+ *   - a private block: nothing.
+ * Sequences are taken in order b = 0, 1, ..., so when several rows share one
+ * block, all but the last of them copy and the last writes in place.
+ * *num_pairs receives the number of copies.  All-or-nothing: when the pool
+ * cannot supply every block the step needs, PKV_ERR_NO_BLOCKS and nothing
+ * changes.  PKV_ERR_INVALID_ARG for p past the row or an entry that is not an
+ * allocated block.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_prepare_append(pkv_pool* pool, int32_t* block_tables, int batch, int max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t* src_blocks, int32_t* dst_blocks,
+                              int32_t* num_pairs);
+
+/* Block copy on the device (the data movement of copy-on-write): for each
+ * i < num_pairs, physical block dst_blocks[i] of k_cache and of v_cache takes
+ * the contents of block src_blocks[i], all heads and all rows; a bit-exact
+ * copy of num_kv_heads * block_size * head_dim elements of elt_bytes bytes
+ * (2 for fp16/bf16 caches, 1 for E4M3) per block and cache.  src_blocks and
+ * dst_blocks are device int32 arrays.  A pair with an id outside
+ * [0, num_blocks) is skipped and reported as PKV_ERR_OOB in err_flag.  The
+ * destinations must be distinct and none may be a source (the pairs
+ * pkv_prepare_append returns are); otherwise the result is undefined.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_copy_blocks(const int32_t* src_blocks, const int32_t* dst_blocks, int64_t num_pairs, void* k_cache,
+                           void* v_cache, int64_t num_blocks, int num_kv_heads, int head_dim, int block_size,
+                           int elt_bytes, int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

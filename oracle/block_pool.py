@@ -114,6 +114,40 @@ class SequenceTable:
             self.blocks.append(block_id)
         self.length = n_blocks * self.pool.block_size
 
+    def fork(self) -> "SequenceTable":
+        """A new sequence that shares every block of this one: a beam-search
+        branch or a parallel sample ("Series 03 ..." section 3.3: branches
+        share the prefix blocks and nothing is copied).  Same length, same
+        physical blocks, each block's reference count one higher."""
+        child = SequenceTable(self.pool)
+        for block_id in self.blocks:
+            self.pool.incref(block_id)
+            child.blocks.append(block_id)
+        child.length = self.length
+        return child
+
+    def prepare_write(self, position: int):
+        """Copy-on-write before writing the token at logical ``position``
+        ("Series 03 ..." section 3.3: when a branch writes its first token of
+        its own into a shared block, a new block is taken, the old contents
+        are copied into it and the token is written there; the other branches
+        keep the old block).  If the block holding ``position`` is shared
+        (reference count > 1), take a fresh block, point this table at it,
+        drop one reference from the old block and return ``(old, new)``: the
+        caller copies block ``old`` into block ``new`` before writing.
+        A private block needs nothing: None.  On exhaustion nothing changes
+        and PoolExhausted is raised."""
+        logical_block = position // self.pool.block_size
+        if not (0 <= logical_block < len(self.blocks)):
+            raise ValueError(f"position {position} lies outside the reserved blocks")
+        old = self.blocks[logical_block]
+        if self.pool.refcount(old) <= 1:
+            return None
+        new = self.pool.alloc()
+        self.pool.decref(old)
+        self.blocks[logical_block] = new
+        return old, new
+
     def release(self) -> None:
         for block_id in self.blocks:
             self.pool.decref(block_id)

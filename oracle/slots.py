@@ -43,3 +43,12 @@ def append_rows(cache: np.ndarray, new_rows: np.ndarray, slots) -> None:
             continue
         blk, off = divmod(int(slot), block_size)
         cache[blk, :, off, :] = new_rows[t]
+
+
+def copy_blocks(cache: np.ndarray, pairs) -> None:
+    """Copy-on-write data movement: for each (src, dst) in order, physical
+    block dst of the cache takes the contents of block src, all heads and all
+    rows ("Series 03 ..." section 3.3: the old block's contents are copied
+    into the newly taken block).  Raw bit patterns, so exact by construction."""
+    for src, dst in pairs:
+        cache[int(dst)] = cache[int(src)]

@@ -22,6 +22,7 @@ __all__ = [
     "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8", "pkv_decode_step_host",
     "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_step", "pkv_paged_decode_step_fp8",
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
+    "pkv_copy_blocks", "pkv_prepare_append",
 ]
 
 PKV_F16 = 0
@@ -63,6 +64,9 @@ _SIGS = {
     "pkv_pool_num_free": (_i64, [_p]),
     "pkv_pool_refcount": (C.c_int32, [_p, C.c_int32]),
     "pkv_blocks_needed": (_i64, [_i64, _i]),
+    "pkv_pool_cow": (_i, [_p, C.c_int32, C.POINTER(C.c_int32)]),
+    "pkv_prepare_append": (_i, [_p, _p, _i, _i, _p, _p, _p, C.POINTER(C.c_int32)]),
+    "pkv_copy_blocks": (_i, [_p, _p, _i64, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -229,6 +233,32 @@ def pkv_decode_step_host(h_q, h_k_new, h_v_new, h_block_tables, h_context_lens, 
         workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
 
 
+def pkv_copy_blocks(src_blocks, dst_blocks, k_cache, v_cache, *, err_flag=None, stream=None) -> None:
+    """Copy-on-write block copy on the device: block dst_blocks[i] of both
+    caches takes block src_blocks[i] (int32 device tensors of equal length)."""
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_copy_blocks", lib.pkv_copy_blocks(
+        _ptr(src_blocks), _ptr(dst_blocks), src_blocks.numel(), _ptr(k_cache), _ptr(v_cache), nb, hkv, d, bs,
+        k_cache.element_size(), _ptr(err_flag), _stream(stream)))
+
+
+def pkv_prepare_append(pool: "BlockPool", block_tables, context_lens):
+    """Host side of one decode step over shared blocks (pkv_prepare_append):
+    updates the int32 host array block_tables [batch, max_blocks] in place and
+    returns the copy pairs (src, dst) as two int32 numpy arrays."""
+    import numpy as np
+    assert block_tables.dtype == np.int32 and block_tables.flags["C_CONTIGUOUS"]
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    batch, max_blocks = block_tables.shape
+    src = np.empty(max(batch, 1), dtype=np.int32)
+    dst = np.empty(max(batch, 1), dtype=np.int32)
+    n = C.c_int32(0)
+    _check("pkv_prepare_append", lib.pkv_prepare_append(
+        pool._h, block_tables.ctypes.data, batch, max_blocks, lens.ctypes.data, src.ctypes.data,
+        dst.ctypes.data, C.byref(n)))
+    return src[:n.value].copy(), dst[:n.value].copy()
+
+
 def pkv_blocks_needed(num_tokens: int, block_size: int = 16) -> int:
     return lib.pkv_blocks_needed(num_tokens, block_size)
 
@@ -265,3 +295,8 @@ class BlockPool:
 
     def refcount(self, block_id: int) -> int:
         return lib.pkv_pool_refcount(self._h, block_id)
+
+    def cow(self, block_id: int) -> int:
+        out = C.c_int32(-1)
+        _check("pkv_pool_cow", lib.pkv_pool_cow(self._h, block_id, C.byref(out)))
+        return out.value

@@ -1,4 +1,5 @@
-// Slot mapping and KV append kernels (sm_103a) and their C-ABI entry points.
+// Slot mapping, KV append and copy-on-write block copy kernels (sm_103a) and
+// their C-ABI entry points.
 //
 // Slot of token t: table[b][p / 16] * 16 + p % 16 (the block-table lookup of
 // "Series 03: why the KV cache eats memory, and how PagedAttention pages it",
@@ -7,6 +8,9 @@
 // E4M3 cache of "KV cache capacity planning ..." section 4, as
 // E4M3_RN_satfinite(fl32(x) / scale[h]).
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
 
 #include "host_util.h"
 #include "pkv_common.cuh"
@@ -103,6 +107,88 @@ __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint
     k_cache[dst] = packed;
 }
 
+// Copy-on-write data movement: block dst[i] of both caches takes block
+// src[i].  The copy is staged through shared memory by TMA: the work is cut
+// into (pair, cache, chunk) items of `chunk` bytes, thread block c takes items
+// c, c + grid, ..., and one thread keeps kCopyStages 1-D bulk loads (global ->
+// shared, completion on an mbarrier per stage) and bulk stores (shared ->
+// global, bulk groups) in flight.  A stage is reloaded only after the store
+// that read it has finished reading (bulk wait_group.read).
+constexpr int kCopyStages = 6;
+constexpr int kCopyChunkMax = 16384;
+
+__global__ void __launch_bounds__(32) copy_blocks_kernel(const int32_t* __restrict__ src,
+                                                         const int32_t* __restrict__ dst, int64_t n_pairs,
+                                                         char* k_cache, char* v_cache, int64_t num_blocks,
+                                                         int64_t block_bytes, int chunk, int chunks_per_block,
+                                                         int32_t* err) {
+  extern __shared__ __align__(128) unsigned char cp_smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(cp_smem + static_cast<size_t>(kCopyStages) * chunk);
+  pdl_wait_and_release();
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kCopyStages; ++s) mbar_init(&full[s], 1);
+  fence_mbar_init();
+  const int64_t per_pair = 2ll * chunks_per_block;
+  const int64_t items = n_pairs * per_pair;
+  const int64_t mine = items > blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint64_t pol = policy_evict_first();
+  // item k of this block: source and destination addresses; false for a pair out of range
+  auto locate = [&](int64_t k, const char*& from, char*& to) -> bool {
+    const int64_t item = blockIdx.x + k * gridDim.x;
+    const int64_t pair = item / per_pair;
+    const int64_t rem = item - pair * per_pair;
+    const int32_t s = src[pair], d = dst[pair];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+      if (rem == 0) record_error(err, PKV_ERR_OOB);
+      return false;
+    }
+    char* base = rem >= chunks_per_block ? v_cache : k_cache;
+    const int64_t off = (rem % chunks_per_block) * chunk;
+    from = base + s * block_bytes + off;
+    to = base + d * block_bytes + off;
+    return true;
+  };
+  uint32_t live = 0;   // bit s: stage s holds a real load
+  auto load = [&](int64_t k) {
+    const int s = static_cast<int>(k % kCopyStages);
+    const char* from;
+    char* to;
+    if (locate(k, from, to)) {
+      mbar_arrive_expect_tx(&full[s], chunk);
+      bulk_g2s(cp_smem + static_cast<size_t>(s) * chunk, from, chunk, &full[s], pol);
+      live |= 1u << s;
+    } else {
+      mbar_arrive(&full[s]);   // completes the phase with no bytes, so parities stay in step
+      live &= ~(1u << s);
+    }
+  };
+  for (int64_t k = 0; k < mine && k < kCopyStages; ++k) load(k);
+  int64_t k = 0;
+  for (; k < mine; ++k) {
+    const int s = static_cast<int>(k % kCopyStages);
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kCopyStages) & 1), err)) break;
+    const char* from;
+    char* to;
+    if (((live >> s) & 1u) && locate(k, from, to)) bulk_s2g(to, cp_smem + static_cast<size_t>(s) * chunk, chunk);
+    bulk_commit_group();
+    // reload the previous item's stage once its store has read it
+    if (k >= 1 && k - 1 + kCopyStages < mine) {
+      bulk_wait_group_read<1>();
+      load(k - 1 + kCopyStages);
+    }
+  }
+  if (k < mine) {
+    // a load never completed: wait (bounded) for the loads still in flight
+    // before the block's shared memory goes away
+    const unsigned long long deadline = global_ns() + kWaitLimitNs;
+    for (int64_t j = k; j < mine && j < k + kCopyStages; ++j) {
+      const int s = static_cast<int>(j % kCopyStages);
+      mbar_wait_until(&full[s], static_cast<uint32_t>((j / kCopyStages) & 1), deadline);
+    }
+  }
+  bulk_wait_group<0>();
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -173,4 +259,47 @@ extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, co
                                    reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale,
                                    v_scale, num_blocks * kBlockSize, num_kv_heads, chunks, err_flag);
   return cuda_failed(e, "kv_append_fp8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
+}
+
+extern "C" pkv_status pkv_copy_blocks(const int32_t* src_blocks, const int32_t* dst_blocks, int64_t num_pairs,
+                                      void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
+                                      int head_dim, int block_size, int elt_bytes, int32_t* err_flag, void* stream) {
+  if (num_pairs < 0 || num_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
+  if (elt_bytes != 1 && elt_bytes != 2) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!src_blocks || !dst_blocks || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  const int64_t block_bytes = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * elt_bytes;
+  if (block_bytes % 16) return PKV_ERR_UNSUPPORTED;
+  // chunk: the largest piece of at most kCopyChunkMax bytes that cuts a block evenly in multiples of 16
+  int64_t pieces = (block_bytes + kCopyChunkMax - 1) / kCopyChunkMax;
+  while (block_bytes % pieces || (block_bytes / pieces) % 16) ++pieces;
+  const int chunk = static_cast<int>(block_bytes / pieces);
+  const size_t smem = static_cast<size_t>(kCopyStages) * chunk + 8 * kCopyStages;
+  int dev = 0, sms = 0;
+  if (cuda_failed(cudaGetDevice(&dev), "cudaGetDevice") ||
+      cuda_failed(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"))
+    return PKV_ERR_CUDA;
+  static std::mutex mu;
+  static bool attr_done[64] = {};
+  if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_done[dev]) {
+      if (cuda_failed(cudaFuncSetAttribute(copy_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kCopyStages) * kCopyChunkMax + 8 * kCopyStages),
+                      "cudaFuncSetAttribute"))
+        return PKV_ERR_CUDA;
+      attr_done[dev] = true;
+    }
+  }
+  // two blocks per SM (each ~96 KiB of stages in flight)
+  const int64_t items = num_pairs * 2 * pieces;
+  const int64_t grid = std::min<int64_t>(items, 2ll * sms);
+  const cudaError_t e =
+      launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(32), smem,
+                 static_cast<cudaStream_t>(stream), src_blocks, dst_blocks, num_pairs, static_cast<char*>(k_cache),
+                 static_cast<char*>(v_cache), num_blocks, block_bytes, chunk, static_cast<int>(pieces), err_flag);
+  return cuda_failed(e, "copy_blocks_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }

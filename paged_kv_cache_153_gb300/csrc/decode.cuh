@@ -434,11 +434,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   // grid reads that slot from the cache: the consumer that processes the
   // last block of (b, g) patches the row in shared memory instead (below).
   // The consumer warps do the writes; the producer starts streaming at once.
+  // Chunks are dealt to thread blocks first (chunk c to block c mod grid), so
+  // every block carries an equal share of this start-up work.
   using NT = std::conditional_t<T::kEsz == 1, QT, KV>;   // element type of the new rows
   if (p.k_new != nullptr && warp < NW) {
     constexpr int kChunks = D / 8;                           // 8 input elements per chunk
     const int64_t total = 2ll * p.batch * Hkv * kChunks;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * (NW * 32) + tid; idx < total;
+    for (int64_t idx = static_cast<int64_t>(tid) * gridDim.x + blockIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * (NW * 32)) {
       int64_t x = idx;
       const int c = static_cast<int>(x % kChunks);

@@ -24,6 +24,11 @@ planning article):
               per-KV-head scales; batch 32: 29 contexts of 2048 and 3 of 65536
               (positions drawn from the seed); partitions of 512 tokens.
 
+Copy-on-write inputs (``beam_inputs``, ``make_beam``, ``copy_pairs``): random
+pools, queries and new rows for a beam search over shared prompts, and random
+disjoint block pairs for block copies; the tables and copies themselves come
+from the block pool under test.
+
 Conventions of every workload:
   * ``context_lens[b]`` counts the tokens attended AFTER the step's append; the
     pool already holds positions 0..ctx-2 and the step appends position ctx-1
@@ -243,6 +248,82 @@ def make(name: str, seed: int | None = None) -> Workload:
         return build(name, batch=32, n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="bf16",
                      kv_dtype="e4m3", context_lens=ctx, seed=seed, partition_tokens=512)
     raise KeyError(name)
+
+
+# ----------------------------------------------------------------------------
+# copy-on-write inputs
+# ----------------------------------------------------------------------------
+@dataclass
+class BeamInputs:
+    """Random data for one decode step of a beam search over shared prompts.
+
+    ``n_prompts`` prompts of ``prompt_lens[p]`` tokens; each is followed by
+    ``beams`` branches that share its blocks, and sequence b = p * beams + j
+    is branch j of prompt p.  Every branch appends one token at position
+    prompt_lens[p] in this step (its context after the append is
+    prompt_lens[p] + 1).  The block tables are NOT laid out here: the caller's
+    block pool takes the prompt blocks (prompt 0 first) and the branches share
+    them, so the tables and the copies follow from the pool under test."""
+    name: str
+    n_prompts: int
+    beams: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    dtype: str
+    scale: float
+    num_blocks: int
+    prompt_lens: np.ndarray        # [n_prompts] int32
+    q: np.ndarray                  # [B, Hq, d] 16-bit bits, B = n_prompts * beams
+    k_pool: np.ndarray             # [NB, Hkv, 16, d] 16-bit bits (every block random)
+    v_pool: np.ndarray
+    k_new: np.ndarray              # [B, Hkv, d]
+    v_new: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return self.n_prompts * self.beams
+
+
+def beam_inputs(name: str, *, n_prompts: int, beams: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                dtype: str, prompt_lens, seed: int, spare_blocks: int | None = None) -> BeamInputs:
+    """Pool = the prompts' blocks + ``spare_blocks`` (default: two per branch)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = np.asarray(prompt_lens, dtype=np.int32)
+    batch = n_prompts * beams
+    spare = 2 * batch if spare_blocks is None else spare_blocks
+    num_blocks = int(sum(_nblocks(n) for n in lens) + spare)
+    return BeamInputs(
+        name=name, n_prompts=n_prompts, beams=beams, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads,
+        head_dim=head_dim, dtype=dtype, scale=1.0 / math.sqrt(head_dim), num_blocks=num_blocks,
+        prompt_lens=lens,
+        q=_normal_bits(rng, (batch, n_q_heads, head_dim), dtype),
+        k_pool=_normal_bits(rng, (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim), dtype),
+        v_pool=_normal_bits(rng, (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim), dtype),
+        k_new=_normal_bits(rng, (batch, n_kv_heads, head_dim), dtype),
+        v_new=_normal_bits(rng, (batch, n_kv_heads, head_dim), dtype),
+        meta={"seed": seed})
+
+
+def make_beam(seed: int = 1100) -> BeamInputs:
+    """8 prompts x 8 branches (64 sequences), Llama-3-8B-like heads (32 query /
+    8 KV, d 128, bf16), prompt lengths U{1000..3000}."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    lens = rng.integers(1000, 3000, size=8, endpoint=True)
+    return beam_inputs("beam", n_prompts=8, beams=8, n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="bf16",
+                       prompt_lens=lens, seed=seed)
+
+
+def copy_pairs(num_blocks: int, n_pairs: int, seed: int):
+    """``n_pairs`` (src, dst) block pairs with distinct sources, distinct
+    destinations and no destination among the sources, drawn as one random
+    permutation of the pool (int32 arrays)."""
+    if 2 * n_pairs > num_blocks:
+        raise ValueError("the pool holds fewer than 2 * n_pairs blocks")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    return perm[:n_pairs].copy(), perm[n_pairs:2 * n_pairs].copy()
 
 
 def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
