@@ -327,6 +327,24 @@ __device__ __noinline__ void patch_new_row(uint32_t kslab, uint32_t vslab, int r
 }
 
 // ---------------------------------------------------------------------------
+// Rows r0..15 of a staged V block lie past the context: their probabilities
+// are zero, but the rows may hold any bit pattern (a NaN would survive the
+// 0 * x of p . V), so they are cleared before p . V.  Whole rows are cleared,
+// which is the same in the swizzled and the linear layout.
+// ---------------------------------------------------------------------------
+template <int D, int ESZ, bool SWZ>
+__device__ __noinline__ void clear_rows(uint32_t vslab, int r0, int lane) {
+  constexpr int kChunks = D * ESZ / 16;    // 16-byte chunks per cache row
+  for (int x = lane; x < (kBlockSize - r0) * kChunks; x += 32) {
+    const int r = r0 + x / kChunks, c = x % kChunks;
+    const uint32_t addr = SWZ ? vslab + (c >> 3) * 2048 + r * 128 + (c & 7) * 16 : vslab + r * D * ESZ + c * 16;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
 // the decode kernel
 // ---------------------------------------------------------------------------
 template <typename QT, typename KV, int D, int G, int NW, bool MMA>
@@ -739,6 +757,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                                               static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
                                               scales[Hkv + d.g], lane);
         }
+        if (n_valid > 0 && n_valid < kBlockSize) clear_rows<D, T::kEsz, true>(vslab, n_valid, lane);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (kFp8) {
 #pragma unroll
@@ -879,6 +898,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                                                static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
                                                scales[Hkv + d.g], lane);
         }
+        if (n_valid > 0 && n_valid < kBlockSize) clear_rows<D, T::kEsz, false>(smem_u32(vslab), n_valid, lane);
 
         // ---- scores: partial dot products over this lane's 8 elements ----
         float part[T::kNV];

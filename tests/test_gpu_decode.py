@@ -238,3 +238,42 @@ def test_full_size_fp8long_sampled(pkv):
         for h in range(g * group, (g + 1) * group):
             ref = oa.attend(q[b, h], keys, values, w.scale)
             assert np.abs(got[b, h] - ref).max() <= gu.FP8_ATOL, (b, h)
+
+
+def _poison_past_context(pool, w, pattern):
+    """Rows of each sequence's last block that lie past its context (the new
+    token's row is position ctx - 1, so rows >= ctx) get a NaN pattern."""
+    for b, n in enumerate(w.context_lens):
+        n = int(n)
+        if n % 16:
+            blk = int(w.block_tables[b][(n - 1) // 16])
+            pool[blk, :, n % 16:, :] = pattern
+
+
+@pytest.mark.parametrize("kind,hq,hkv,head_dim", [("f16", 8, 8, 128), ("bf16", 16, 4, 128), ("bf16", 8, 2, 64),
+                                                  ("e4m3", 16, 4, 128), ("e4m3", 8, 8, 64)])
+@pytest.mark.parametrize("partition", [0, 32])
+def test_garbage_past_the_context_is_ignored(pkv, kind, hq, hkv, head_dim, partition):
+    # The pages' block waste (the unused tail of a sequence's last block) may
+    # hold anything; a NaN there must not reach the output.
+    dtype = "bf16" if kind == "e4m3" else kind
+    w = wl.build("poison", batch=len(RAGGED), n_q_heads=hq, n_kv_heads=hkv, head_dim=head_dim, dtype=dtype,
+                 kv_dtype=kind, context_lens=RAGGED, seed=7 + hq + head_dim)
+    if kind == "e4m3":
+        kc, vc, kn, vn = gu.oracle_fp8_codes(w)
+        _poison_past_context(kc, w, 0x7F)
+        _poison_past_context(vc, w, 0x7F)
+        case = gu.GpuCase(w, codes=(kc, vc))
+        case.step(partition_tokens=partition)
+        slots = gu.oracle_slots(w)
+        gu.osl.append_rows(kc, kn, slots)
+        gu.osl.append_rows(vc, vn, slots)
+        _check(case, gu.oracle_decode(w, kc, vc), fp8=True, label=f"{kind} P{partition}")
+    else:
+        _poison_past_context(w.k_pool, w, 0x7FFF)
+        _poison_past_context(w.v_pool, w, 0x7FFF)
+        case = gu.GpuCase(w)
+        case.step(partition_tokens=partition)
+        kp, vp = gu.oracle_pools_after_append(w)
+        _check(case, gu.oracle_decode(w, kp, vp), label=f"{kind} P{partition}")
+    assert bool(torch.isfinite(case.out).all())
