@@ -34,6 +34,7 @@ slots        slot mapping: logical position -> physical slot.
 append       writing new K/V rows into their slots (a bit copy).
 e4m3         the OCP FP8 E4M3 code table, encoder and decoder.
 attention    paged decode attention and the contiguous (no-cache) comparator.
+prefill      paged prefill / extend attention (causal over the cached context).
 toy_model    a tiny projection model that recomputes K/V from scratch.
 numerics     exact decoding of stored fp16 / bf16 bit patterns to float64.
 
