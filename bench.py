@@ -526,13 +526,135 @@ def run_copy(args, rank: int, local_rank: int) -> dict | None:
     }
 
 
+# ---------------------------------------------------------------------------
+# paged prefill / extend attention (--workload prefill)
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "paged prefill (causal extend attention) TFLOP/s, 1 GPU"
+
+
+def prefill_config(pi) -> dict:
+    return {"workload": f"prefill: {pi.batch} sequences x ({int(pi.cached_lens[0])} cached + {int(pi.new_lens[0])} "
+                        f"new tokens), {pi.n_q_heads} query / {pi.n_kv_heads} KV heads, head_dim {pi.head_dim}, "
+                        f"{pi.dtype}, block 16", "batch": pi.batch, "num_q_heads": pi.n_q_heads,
+            "num_kv_heads": pi.n_kv_heads, "head_dim": pi.head_dim, "new_tokens": int(pi.new_lens.sum()),
+            "cached_tokens": int(pi.cached_lens.sum()), "flops_per_step": pi.flops(),
+            "l2": "K/V of the batch fit in L2 and are re-read by every query tile; no flush (compute-bound)"}
+
+
+def oracle_prefill_rate(pi, budget_s: float) -> tuple[float, str]:
+    """The oracle's prefill rows on the host: FLOP/s over a bounded sample."""
+    from oracle import numerics as on
+    from oracle import prefill as op
+    q = on.bits_to_f64(pi.q, pi.dtype)
+    kc, vc = on.bits_to_f64(pi.k_pool, pi.dtype), on.bits_to_f64(pi.v_pool, pi.dtype)
+    pos = op.prefill_positions(pi.context_lens, pi.cu_seqlens)
+    flops, done, t0 = 0, 0, time.perf_counter()
+    while True:
+        t = (done * 997) % q.shape[0]
+        op.paged_prefill_attention(q, kc, vc, pi.block_tables, pi.context_lens, pi.cu_seqlens, pi.scale, rows=[t])
+        flops += 4 * pi.head_dim * pi.n_q_heads * (pos[t][1] + 1)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return flops / el / 1e12, f"{done} query tokens (all heads), float64, {el:.1f} s on one host thread"
+
+
+def run_prefill(args, rank: int, local_rank: int) -> dict | None:
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import paged_kv_cache_153_gb300 as pkv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pi = wl.make_prefill()
+    stream = torch.cuda.Stream(device=dev)
+    bf = torch.bfloat16
+    with torch.cuda.stream(stream):
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(bf).to(dev)
+        q, kc, vc = up(pi.q), up(pi.k_pool), up(pi.v_pool)
+        tables = torch.from_numpy(pi.block_tables).to(dev)
+        lens = torch.from_numpy(pi.context_lens).to(dev)
+        cu = torch.from_numpy(pi.cu_seqlens).to(dev)
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream.synchronize()
+    mql = int(pi.new_lens.max())
+
+    def step(q_=q, t_=tables, l_=lens, c_=cu):
+        pkv.pkv_paged_prefill_attention(q_, kc, vc, t_, l_, c_, out, scale=pi.scale, max_query_len=mql,
+                                        err_flag=err, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())} during warm-up")
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step()
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    per_ms = t_start.elapsed_time(t_end) / args.steps
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())} in the timed region")
+    tflops = pi.flops() / (per_ms * 1e-3) / 1e12
+    # end to end: queries, tables, lengths and offsets from pinned host memory, the output read back
+    h_q = torch.from_numpy(np.ascontiguousarray(pi.q)).view(bf).pin_memory()
+    h_t = torch.from_numpy(pi.block_tables).pin_memory()
+    h_l, h_c = torch.from_numpy(pi.context_lens).pin_memory(), torch.from_numpy(pi.cu_seqlens).pin_memory()
+    h_out = torch.empty(out.shape, dtype=bf).pin_memory()
+    d_q, d_t, d_l, d_c = torch.empty_like(q), torch.empty_like(tables), torch.empty_like(lens), torch.empty_like(cu)
+
+    def host_step():
+        for d_, h_ in ((d_q, h_q), (d_t, h_t), (d_l, h_l), (d_c, h_c)):
+            d_.copy_(h_, non_blocking=True)
+        step(d_q, d_t, d_l, d_c)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            host_step()
+        n_e2e = max(5, min(args.steps, 100))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        e2e_s = time.perf_counter() - t0
+    if rank != 0:
+        return None
+    peak, kind = 1935.8, "fallback"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        pass
+    return {
+        "metric": PREFILL_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": prefill_config(pi),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "traffic": ncu_traffic("prefill"), "kernel": "paged_prefill_kernel (pkv_paged_prefill_attention), "
+                     "average over the back-to-back calls of the timed region",
+                     "algorithmic_flops_per_launch": pi.flops(), "avg_launch_ms": per_ms,
+                     "peak_kind": f"{kind} dense bf16 (burst)"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "e2e": {"value": pi.flops() * n_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in (h_q, h_t, h_l, h_c))),
+                "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": n_e2e,
+                "path": "queries and tables from pinned host memory, pkv_paged_prefill_attention, output read back"},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow"])
+    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -540,6 +662,30 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == "prefill":
+        pi = wl.make_prefill()
+        if args.impl == "reference":
+            if rank != 0:
+                return
+            rate, sample = oracle_prefill_rate(pi, budget_s=max(1.0, 0.05 * args.steps))
+            print(json.dumps({
+                "impl": "reference", "metric": PREFILL_METRIC, "value": rate, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": pi.flops() / (rate * 1e12) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": prefill_config(pi),
+                "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+                "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+            return
+        res = run_prefill(args, rank, local_rank)
+        if res is not None:
+            if not args.no_cpu_baseline:
+                rate, sample = oracle_prefill_rate(pi, budget_s=10.0)
+                res["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                       "sample": sample}
+            print(json.dumps(res), flush=True)
+        return
 
     if args.workload == "cow":
         if args.impl == "reference":

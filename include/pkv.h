@@ -259,6 +259,34 @@ pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void
                                 size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged prefill / extend attention ("KV Cache, the memory notepad ...",
+ * sections 二-四: prefill attends over the prompt; "Series 03 ...", section 3.1:
+ * K/V through the block table, section 5.1: chunked prefill).  The new tokens
+ * of sequence b are its last n_b = cu_seqlens[b+1] - cu_seqlens[b] positions
+ * (context_lens[b] counts them; the cache must already hold their K/V, e.g.
+ * written by pkv_kv_append).  Token i of sequence b, at position
+ * p = context_lens[b] - n_b + i, attends causally to positions 0..p:
+ *     out[cu_seqlens[b] + i, h] = sum_{j <= p} softmax_j(scale <q, K_j>) V_j
+ * with K_j, V_j of KV head h / G (G = num_q_heads / num_kv_heads in {1, 2, 4,
+ * 8}).  q and out are [T, num_q_heads, 128] of dtype (T = cu_seqlens[batch]);
+ * the caches [num_blocks, num_kv_heads, 16, 128] of the same dtype;
+ * block_tables int32 [batch, max_blocks_per_seq]; context_lens, cu_seqlens
+ * int32 device arrays; max_query_len >= every n_b.  Runs on the tensor cores
+ * (tcgen05, accumulators in tensor memory) with fp32 softmax; P is rounded to
+ * dtype before P.V.  head_dim 128 and block_size 16 only (else
+ * PKV_ERR_UNSUPPORTED).  Device errors in err_flag: PKV_ERR_OOB for a block id
+ * outside [0, num_blocks), more new tokens than context or a context past the
+ * table (that sequence's tile is skipped); PKV_ERR_TIMEOUT if a pipeline wait
+ * exceeds its limit.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       const int32_t* cu_seqlens, int batch, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                       int max_query_len, float scale, void* out, pkv_dtype dtype,
+                                       int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Host-side block pool ("Series 03 ...", sections 3.2-3.3; "What a KV cache
  * is ...", section 3.2): a preallocated set of block ids handed out on demand,
  * with reference counts for blocks shared by several block tables.  Policy: a

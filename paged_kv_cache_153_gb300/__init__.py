@@ -22,7 +22,7 @@ __all__ = [
     "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8", "pkv_decode_step_host",
     "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_step", "pkv_paged_decode_step_fp8",
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
-    "pkv_copy_blocks", "pkv_prepare_append",
+    "pkv_copy_blocks", "pkv_prepare_append", "pkv_paged_prefill_attention",
 ]
 
 PKV_F16 = 0
@@ -67,6 +67,8 @@ _SIGS = {
     "pkv_pool_cow": (_i, [_p, C.c_int32, C.POINTER(C.c_int32)]),
     "pkv_prepare_append": (_i, [_p, _p, _i, _i, _p, _p, _p, C.POINTER(C.c_int32)]),
     "pkv_copy_blocks": (_i, [_p, _p, _i64, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
+    "pkv_paged_prefill_attention": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
+                                         _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -257,6 +259,17 @@ def pkv_prepare_append(pool: "BlockPool", block_tables, context_lens):
         pool._h, block_tables.ctypes.data, batch, max_blocks, lens.ctypes.data, src.ctypes.data,
         dst.ctypes.data, C.byref(n)))
     return src[:n.value].copy(), dst[:n.value].copy()
+
+
+def pkv_paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, cu_seqlens, out, *, scale: float,
+                                max_query_len: int, dtype=None, err_flag=None, stream=None) -> None:
+    """Causal extend attention of the new tokens q [T, Hq, D] over the paged
+    cache (which already holds their K/V)."""
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_paged_prefill_attention", lib.pkv_paged_prefill_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(cu_seqlens),
+        context_lens.numel(), q.shape[1], hkv, d, bs, block_tables.shape[1], nb, max_query_len, scale, _ptr(out),
+        _dtype_code(q, dtype), _ptr(err_flag), _stream(stream)))
 
 
 def pkv_blocks_needed(num_tokens: int, block_size: int = 16) -> int:

@@ -43,7 +43,9 @@
 //    go through the online softmax in registers; p is rounded to the cache's
 //    16-bit type, transposed in registers (movmatrix) into the B operand of
 //    p.V, which accumulates O^T[head_dim x heads] in fp32 with V^T read by
-//    ldmatrix.trans.  The normaliser l sums the same rounded p.
+//    ldmatrix.trans.  For bf16, p is multiplied as hi + lo bf16 parts (one
+//    rounding of p to bf16 can exceed the tolerance on short contexts).  The
+//    normaliser l sums exactly the p that is multiplied.
 //
 // Fused step (k_new != null).  The same launch also appends each sequence's
 // new K/V row at position ctx - 1: thread blocks share the global writes in
@@ -258,17 +260,6 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// two floats -> packed 16-bit pair (lo in the low half), round to nearest even
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, BF16) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, F16) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 // two E4M3 codes (bits 0-15 of w: low byte first) -> packed f16x2, exactly
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   uint32_t r;
@@ -276,15 +267,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   return r;
 }
 
-// 2-D tiled TMA load of a [16 x 128 B] box at (x elements, y rows)
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
 
 // address of 16-byte chunk `chunk` of row `row` in a slab staged as 128B-swizzled
 // [16 x 128 B] sub-tiles (each 2 KiB, 1024-byte aligned)
@@ -791,15 +773,36 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0, ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
         const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
-        const uint32_t x0 = pack2(exp2f(s00 - ref0), exp2f(s01 - ref1), MT{});   // tokens 0..7
-        const uint32_t x1 = pack2(exp2f(s10 - ref0), exp2f(s11 - ref1), MT{});   // tokens 8..15
+        // p in the MMA type.  bf16 keeps 8 significant bits, and one rounding
+        // of p (2^-9 relative) can exceed the 2e-3 tolerance on outputs of a
+        // few keys, so bf16 p is multiplied as hi = bf16(p) plus
+        // lo = bf16(p - hi) (exact to ~2^-17); fp16 p (2^-12) is used as is.
+        constexpr bool kSplitP = std::is_same<MT, BF16>::value;
+        const float e00 = exp2f(s00 - ref0), e01 = exp2f(s01 - ref1);
+        const float e10 = exp2f(s10 - ref0), e11 = exp2f(s11 - ref1);
+        const uint32_t x0 = pack2(e00, e01, MT{});   // tokens 0..7
+        const uint32_t x1 = pack2(e10, e11, MT{});   // tokens 8..15
         const float2 p0 = unpack2(x0, MT{}), p1 = unpack2(x1, MT{});
-        l0 = l0 * a0 + (p0.x + p1.x);
-        l1 = l1 * a1 + (p0.y + p1.y);
+        uint32_t x0l = 0u, x1l = 0u;
+        float2 r0 = make_float2(0.f, 0.f), r1 = make_float2(0.f, 0.f);
+        if constexpr (kSplitP) {
+          x0l = pack2(e00 - p0.x, e01 - p0.y, MT{});
+          x1l = pack2(e10 - p1.x, e11 - p1.y, MT{});
+          r0 = unpack2(x0l, MT{});
+          r1 = unpack2(x1l, MT{});
+        }
+        // l sums exactly what is multiplied
+        l0 = l0 * a0 + ((p0.x + r0.x) + (p1.x + r1.x));
+        l1 = l1 * a1 + ((p0.y + r0.y) + (p1.y + r1.y));
         const bool resc = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
         m0 = mn0;
         m1 = mn1;
         const uint32_t b0 = movmatrix_trans(x0), b1 = movmatrix_trans(x1);
+        uint32_t b0l = 0u, b1l = 0u;
+        if constexpr (kSplitP) {
+          b0l = movmatrix_trans(x0l);
+          b1l = movmatrix_trans(x1l);
+        }
         if (resc) {
 #pragma unroll
           for (int mt = 0; mt < KS; ++mt) {
@@ -828,6 +831,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             uint32_t a[4];
             ldsm_x4_trans(swz_addr(vslab, vrow, 2 * mt + vchunk), a);
             mma16816(o[mt], a, b0, b1, MT{});
+            if constexpr (kSplitP) mma16816(o[mt], a, b0l, b1l, MT{});
           }
         }
         __syncwarp();

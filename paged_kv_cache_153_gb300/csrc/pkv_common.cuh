@@ -7,6 +7,7 @@
 // * 16-bit / E4M3 -> fp32 conversions and the fp32 -> 16-bit output rounding.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -130,6 +131,16 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 2-D tiled TMA load of a [16 x 128 B] box at (x elements, y rows)
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // named barrier among a subset of warps (id 0 is __syncthreads)
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -237,6 +248,18 @@ __device__ __forceinline__ uint2 quant8_e4m3(const void* src, float scale, IN) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) w[e] = e4m3x2_from_f32(__fdiv_rn(x[2 * e], scale), __fdiv_rn(x[2 * e + 1], scale));
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+// two floats -> packed 16-bit pair (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, BF16) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, F16) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // fp32 -> output element, round to nearest even

@@ -24,6 +24,10 @@ planning article):
               per-KV-head scales; batch 32: 29 contexts of 2048 and 3 of 65536
               (positions drawn from the seed); partitions of 512 tokens.
 
+Prefill inputs (``prefill_inputs``, ``make_prefill``): sequences with a
+cached prefix and new tokens after it, random queries and pool, tables from a
+random permutation of the pool.
+
 Copy-on-write inputs (``beam_inputs``, ``make_beam``, ``copy_pairs``): random
 pools, queries and new rows for a beam search over shared prompts, and random
 disjoint block pairs for block copies; the tables and copies themselves come
@@ -324,6 +328,78 @@ def copy_pairs(num_blocks: int, n_pairs: int, seed: int):
     rng = np.random.Generator(np.random.PCG64(seed))
     perm = rng.permutation(num_blocks).astype(np.int32)
     return perm[:n_pairs].copy(), perm[n_pairs:2 * n_pairs].copy()
+
+
+# ----------------------------------------------------------------------------
+# prefill / extend inputs
+# ----------------------------------------------------------------------------
+@dataclass
+class PrefillInputs:
+    """Random data for one prefill (extend) call: sequence b has
+    ``cached_lens[b]`` tokens already in the cache and ``new_lens[b]`` new
+    tokens after them (their K/V rows are already in the pool too, as after
+    the append); q holds the new tokens' queries, packed by cu_seqlens."""
+    name: str
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    dtype: str
+    scale: float
+    num_blocks: int
+    cached_lens: np.ndarray        # [B] int32
+    new_lens: np.ndarray           # [B] int32
+    context_lens: np.ndarray       # [B] int32 = cached + new
+    cu_seqlens: np.ndarray         # [B + 1] int32
+    block_tables: np.ndarray       # [B, max_blocks] int32, -1 padded
+    q: np.ndarray                  # [T, Hq, d] 16-bit bits
+    k_pool: np.ndarray             # [NB, Hkv, 16, d] 16-bit bits
+    v_pool: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.new_lens)
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return self.block_tables.shape[1]
+
+    def flops(self) -> int:
+        """Causal extend attention: 4 d flops per (query token, query head,
+        attended key) -- 2 d for q.K, 2 d for p.V."""
+        n = 0
+        for c, m in zip(self.cached_lens, self.new_lens):
+            c, m = int(c), int(m)
+            n += m * c + m * (m + 1) // 2          # sum over new tokens of (position + 1)
+        return 4 * self.head_dim * self.n_q_heads * n
+
+
+def prefill_inputs(name: str, *, cached_lens, new_lens, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                   dtype: str, seed: int, free_fraction: float = 0.05) -> PrefillInputs:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cached = np.asarray(cached_lens, dtype=np.int32)
+    new = np.asarray(new_lens, dtype=np.int32)
+    ctx = cached + new
+    blocks = [_nblocks(c) for c in ctx]
+    num_blocks = max(1, math.ceil(sum(blocks) * (1.0 + free_fraction)))
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    tables = _tables_from_ids(perm, blocks, max(blocks + [1]))
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    return PrefillInputs(
+        name=name, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim, dtype=dtype,
+        scale=1.0 / math.sqrt(head_dim), num_blocks=int(num_blocks), cached_lens=cached, new_lens=new,
+        context_lens=ctx.astype(np.int32), cu_seqlens=cu, block_tables=tables,
+        q=_normal_bits(rng, (int(cu[-1]), n_q_heads, head_dim), dtype),
+        k_pool=_normal_bits(rng, (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim), dtype),
+        v_pool=_normal_bits(rng, (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim), dtype),
+        meta={"seed": seed})
+
+
+def make_prefill(seed: int = 1300) -> PrefillInputs:
+    """Chunked prefill of 4 sequences: 2048 tokens cached, 2048 new tokens
+    each; Llama-3-8B-like heads (32 query / 8 KV, d 128, bf16)."""
+    return prefill_inputs("prefill", cached_lens=[2048] * 4, new_lens=[2048] * 4, n_q_heads=32, n_kv_heads=8,
+                          head_dim=128, dtype="bf16", seed=seed)
 
 
 def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:

@@ -277,3 +277,16 @@ def test_garbage_past_the_context_is_ignored(pkv, kind, hq, hkv, head_dim, parti
         kp, vp = gu.oracle_pools_after_append(w)
         _check(case, gu.oracle_decode(w, kp, vp), label=f"{kind} P{partition}")
     assert bool(torch.isfinite(case.out).all())
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 4), (16, 2), (8, 4)])
+def test_bf16_short_contexts(pkv, hq, hkv):
+    # few keys: a single rounding of the softmax weights to bf16 would be
+    # visible against the tolerance; the tensor-core path multiplies them exactly
+    lens = list(range(2, 34)) * 2
+    w = wl.build("short-bf16", batch=len(lens), n_q_heads=hq, n_kv_heads=hkv, head_dim=128, dtype="bf16",
+                 kv_dtype="bf16", context_lens=lens, seed=hq + hkv)
+    case = gu.GpuCase(w)
+    case.step()
+    kp, vp = gu.oracle_pools_after_append(w)
+    _check(case, gu.oracle_decode(w, kp, vp), label=f"short bf16 {hq}/{hkv}")
