@@ -17,7 +17,9 @@
 // loads of [16 rows x 128 B] boxes into the 128-byte swizzled K-major layout
 // the tensor cores read.  Per key tile:
 //   S = Q K^T     tcgen05.mma kind::f16, M = N = 128, 8 k-steps of 16, fp32 in TMEM
-//   softmax       4 warps, one row per thread: tcgen05.ld of the S row, mask,
+//   softmax       8 warps, two threads per row (warps w and w + 4 share TMEM
+//                 lane quarter w % 4; each takes 64 of the 128 columns and both
+//                 take the row maximum over all of them): tcgen05.ld of S, mask,
 //                 online max / sum in the log2 domain, P stored to shared
 //                 memory in the input type (K-major, swizzled); when a row's
 //                 max grows its O row in TMEM is rescaled (ld, scale, st)
@@ -28,8 +30,13 @@
 //                 passes): P is then exact to ~2^-17 relative, where a single
 //                 bf16 rounding (2^-9) could exceed the 2e-3 tolerance on
 //                 outputs of a few keys.  fp16 P (2^-12) needs one pass.
-// Warp roles: warps 0-3 softmax and epilogue, warp 4 TMA producer (a 2-stage
-// K/V ring), warp 5 TMEM owner and MMA issuer (one elected lane).  Every wait
+// Warp roles: warps 0-7 softmax and epilogue, warp 8 TMA producer (a 2-stage
+// ring with separate K and V barriers: K of tile j + 2 is loaded as soon as
+// Q K^T of tile j is done, V once P V of tile j is), warp 9 TMEM owner and
+// MMA issuer (one elected lane).  S has two
+// TMEM buffers: the MMA warp issues Q K^T of tile j+1 before it waits for the
+// softmax of tile j, so the tensor cores compute the next scores while the
+// softmax warps work.  Every wait
 // is bounded; on expiry the block records PKV_ERR_TIMEOUT, drains what it has
 // in flight and frees its TMEM.
 #include <cuda.h>
@@ -64,8 +71,9 @@ constexpr int kPM = 128;                  // query rows per tile
 constexpr int kPN = 128;                  // keys per tile
 constexpr int kPD = 128;                  // head_dim
 constexpr int kTile = kPM * kPD * 2;      // bytes of a 128 x 128 16-bit tile (Q, P, K or V)
-constexpr int kPThreads = 192;
-constexpr int kTmemCols = 256;            // S: columns 0-127, O: 128-255
+constexpr int kPThreads = 320;           // 8 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kSoftmax = 256;            // softmax threads: 2 per query row
+constexpr int kTmemCols = 512;            // S of even tiles: 0-127, O: 128-255, S of odd tiles: 256-383
 constexpr size_t kPrefillSmem = 7 * static_cast<size_t>(kTile) + 256 + 1024;
 
 // offsets in the 1024-aligned shared block: Q | P (hi part) | P (lo part) | K0 V0 | K1 V1 | barriers
@@ -104,6 +112,13 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -160,15 +175,17 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   extern __shared__ unsigned char psm_raw[];
   unsigned char* sm = psm_raw + ((1024 - (smem_u32(psm_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint64_t* kv_full = bars;          // [2]
-  uint64_t* kv_empty = bars + 2;     // [2]
-  uint64_t* s_full = bars + 4;
-  uint64_t* p_full = bars + 5;       // 128 arrivals
-  uint64_t* pv_done = bars + 6;
-  uint64_t* q_ready = bars + 7;      // 128 arrivals
-  uint64_t* mma_idle = bars + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 10);
+  uint64_t* k_full = bars;           // [2] per stage: K of the stage's tile landed
+  uint64_t* v_full = bars + 2;       // [2] V landed
+  uint64_t* k_empty = bars + 4;      // [2] Q K^T of the stage's tile done: K may be reloaded
+  uint64_t* v_empty = bars + 6;      // [2] P V done: V may be reloaded
+  uint64_t* s_full = bars + 8;       // [2], one per S buffer
+  uint64_t* p_full = bars + 10;      // kSoftmax arrivals
+  uint64_t* pv_done = bars + 11;
+  uint64_t* q_ready = bars + 12;     // kSoftmax arrivals
+  uint64_t* mma_idle = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 15);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
@@ -190,7 +207,7 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   const int n_tiles = last_pos / kPN + 1;
   const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
 
-  if (warp == 5) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
@@ -199,13 +216,16 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, kPM);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, kSoftmax);
     mbar_init(pv_done, 1);
-    mbar_init(q_ready, kPM);
+    mbar_init(q_ready, kSoftmax);
     mbar_init(mma_idle, 1);
     fence_mbar_init();
   }
@@ -213,11 +233,13 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_o = tmem + kPN;
+  const uint32_t t_o = tmem + kPN;
+  auto t_s = [&](int j) -> uint32_t { return tmem + ((j & 1) ? 2 * kPN : 0); };
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ============================ softmax / epilogue ============================
-    const int r = tid;                                 // row = TMEM lane
+    const int r = tid & (kPM - 1);                     // row = TMEM lane
+    const int half = tid >> 7;                         // columns [64 half, 64 half + 64) of S, P and O
     const int tok = i0 + r / G, head = g * G + r % G;
     const bool row_live = tok < i1;
     const int pos = row_live ? q_start + tok : -1;
@@ -227,7 +249,7 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
                                                         ((static_cast<int64_t>(cu0) + tok) * p.n_q_heads + head) *
                                                             kPD * 2);
 #pragma unroll
-      for (int c = 0; c < kPD / 8; ++c) {
+      for (int c = 8 * half; c < 8 * half + 8; ++c) {
         const uint4 v = row_live ? src[c] : make_uint4(0, 0, 0, 0);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffQ) + tile_off(r, c)),
                      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -236,50 +258,41 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
     }
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
       // waits are made warp-uniform: the tcgen05.ld / st below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, p.err))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err))) { ok = false; break; }
       tc_fence_after();
-      float s[kPN];
-#pragma unroll
-      for (int c0 = 0; c0 < kPN; c0 += 32) tmem_ld32(t_s + lane_base + c0, s + c0);
-      // mask (causal, and keys past the context) and scale into the log2 domain
+      // Two passes over the S row in chunks of 32 columns, re-read from TMEM
+      // (a compact loop: the fully unrolled row did not fit the instruction
+      // cache).  Only tiles that reach past a row's position need the mask.
+      const bool masked = __any_sync(0xffffffffu, j * kPN + kPN - 1 > pos);   // (for pass 1; pass 2 re-tests)
       float mx = -INFINITY;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kPN; c0 += 32) {
+        float v[32];
+        tmem_ld32(t_s(j) + lane_base + c0, v);
+        if (masked) {
 #pragma unroll
-      for (int c = 0; c < kPN; ++c) {
-        const int key = j * kPN + c;
-        s[c] = (key <= pos) ? s[c] * p.qk_scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = exp2f(m_run - ref);
-      constexpr bool kSplit = std::is_same<QT, BF16>::value;
-      uint32_t pk[kPN / 2], pl[kSplit ? kPN / 2 : 1];
-      float psum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kPN; c += 2) {
-        const float e0 = exp2f(s[c] - ref), e1 = exp2f(s[c + 1] - ref);
-        pk[c / 2] = pack2(e0, e1, QT{});
-        const float2 back = unpack2(pk[c / 2], QT{});
-        if constexpr (kSplit) {
-          pl[c / 2] = pack2(e0 - back.x, e1 - back.y, QT{});
-          const float2 lo = unpack2(pl[c / 2], QT{});
-          psum += (back.x + lo.x) + (back.y + lo.y);   // the sum of what is multiplied
-        } else {
-          psum += back.x + back.y;
+          for (int i = 0; i < 32; ++i) v[i] = (j * kPN + c0 + i <= pos) ? v[i] : -INFINITY;
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
       }
+      // scores in the log2 domain: s * scale * log2(e) (the scale is positive,
+      // so the maximum commutes with it)
+      const float m_new = fmaxf(m_run, mx * p.qk_scale_log2);
+      const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m_run - ref);
       // O and the P buffer are free once the previous p.V has completed
       if (j > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, p.err))) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < kPD; c0 += 32) {
+          for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float o[32];
             tmem_ld32(t_o + lane_base + c0, o);
 #pragma unroll
@@ -288,32 +301,65 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
           }
         }
       }
+      constexpr bool kSplit = std::is_same<QT, BF16>::value;
+      float psum = 0.f;
+      const float nref = -ref;
+#pragma unroll 1
+      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+        float v[32];
+        tmem_ld32(t_s(j) + lane_base + c0, v);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float e0 = ex2_approx(fmaf(v[i], p.qk_scale_log2, nref));
+          float e1 = ex2_approx(fmaf(v[i + 1], p.qk_scale_log2, nref));
+          if (masked) {
+            e0 = (j * kPN + c0 + i <= pos) ? e0 : 0.f;
+            e1 = (j * kPN + c0 + i + 1 <= pos) ? e1 : 0.f;
+          }
+          psum += e0 + e1;
+          hi[i / 2] = pack2(e0, e1, QT{});
+          if constexpr (kSplit) {
+            const float2 b = unpack2(hi[i / 2], QT{});
+            lo[i / 2] = pack2(e0 - b.x, e1 - b.y, QT{});
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t off = tile_off(r, c0 / 8 + c);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffP) + off),
+                       "r"(hi[4 * c]), "r"(hi[4 * c + 1]), "r"(hi[4 * c + 2]), "r"(hi[4 * c + 3])
+                       : "memory");
+          if constexpr (kSplit)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffPlo) + off),
+                         "r"(lo[4 * c]), "r"(lo[4 * c + 1]), "r"(lo[4 * c + 2]), "r"(lo[4 * c + 3])
+                         : "memory");
+        }
+      }
+      // l sums the fp32 weights (the multiplied hi + lo, or fp16, parts match
+      // them to ~2^-17 / 2^-12 relative)
       l_run = l_run * alpha + psum;
       m_run = m_new;
-#pragma unroll
-      for (int c = 0; c < kPN / 8; ++c) {
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffP) + tile_off(r, c)),
-                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-        if constexpr (kSplit)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffPlo) + tile_off(r, c)),
-                       "r"(pl[4 * c]), "r"(pl[4 * c + 1]), "r"(pl[4 * c + 2]), "r"(pl[4 * c + 3])
-                       : "memory");
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
     }
     if (!ok) *abort_flag = 1;
-    // epilogue: out = O / l
+    // epilogue: out = O / l.  The two threads of a row hold the sums of their
+    // halves; they meet in the P buffer, free once the last p.V is done.
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && __all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1, p.err))) {
+    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1, p.err));
+    float* lx = reinterpret_cast<float*>(sm + kOffP);
+    lx[half * kPM + r] = l_run;
+    named_bar_sync(1, kSoftmax);
+    const float l_tot = l_run + lx[(1 - half) * kPM + r];
+    if (fin) {
       tc_fence_after();
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
       auto* dst = reinterpret_cast<uint4*>(static_cast<typename QT::storage*>(p.out) +
                                            ((static_cast<int64_t>(cu0) + tok) * p.n_q_heads + head) * kPD);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kPD; c0 += 32) {
+      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
         float o[32];
         tmem_ld32(t_o + lane_base + c0, o);
         if (row_live) {
@@ -328,43 +374,60 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     } else {
       *abort_flag = 1;
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ============================ TMA producer ============================
     const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by the other query tiles
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    int j = 0;
+    int j = 0, issued_k = 0, issued_v = 0;
     for (; j < n_tiles && !*abort_flag; ++j) {
       const int s = j & 1;
-      if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, p.err)) {
-        *abort_flag = 1;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], 2 * kTile);
-      __syncwarp();
+      int id = -1;
       if (lane < kPN / kBlockSize) {
         const int blk = j * (kPN / kBlockSize) + lane;
-        int id = (blk < nblk) ? row[blk] : -1;
+        id = (blk < nblk) ? row[blk] : -1;
         if (blk < nblk && (id < 0 || id >= p.num_blocks)) {
           record_error(p.err, PKV_ERR_OOB);
           id = -1;
         }
-        // a block past the context (or a bad id) is read from rows outside the
-        // tensor, which TMA fills with zeros
-        const int y = (id >= 0) ? (id * p.n_kv_heads + g) * kBlockSize : -2 * kBlockSize;
-        unsigned char* kd = sm + kOffKV + 2 * s * kTile + lane * 2048;
-        unsigned char* vd = kd + kTile;
+      }
+      // a block past the context (or a bad id) is read from rows outside the
+      // tensor, which TMA fills with zeros
+      const int y = (id >= 0) ? (id * p.n_kv_heads + g) * kBlockSize : -2 * kBlockSize;
+      unsigned char* kd = sm + kOffKV + 2 * s * kTile + lane * 2048;
+      unsigned char* vd = kd + kTile;
+      // K, then V, each after its previous use in this stage is done
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, p.err))) {
+        *abort_flag = 1;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[s], kTile);
+      __syncwarp();
+      if (lane < kPN / kBlockSize) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tma_load_2d(kd + h * (kTile / 2), &p.tmap_k, h * 64, y, &kv_full[s], pol);
-          tma_load_2d(vd + h * (kTile / 2), &p.tmap_v, h * 64, y, &kv_full[s], pol);
-        }
+        for (int h = 0; h < 2; ++h) tma_load_2d(kd + h * (kTile / 2), &p.tmap_k, h * 64, y, &k_full[s], pol);
       }
       __syncwarp();
+      issued_k = j + 1;
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, p.err))) {
+        *abort_flag = 1;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[s], kTile);
+      __syncwarp();
+      if (lane < kPN / kBlockSize) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tma_load_2d(vd + h * (kTile / 2), &p.tmap_v, h * 64, y, &v_full[s], pol);
+      }
+      __syncwarp();
+      issued_v = j + 1;
     }
     if (*abort_flag && lane == 0) {
       // loads this warp issued that nobody consumed: wait for them (bounded)
       const unsigned long long deadline = global_ns() + kWaitLimitNs;
-      for (int jj = max(0, j - 2); jj < j; ++jj) mbar_wait_until(&kv_full[jj & 1], (jj >> 1) & 1, deadline);
+      for (int jj = max(0, issued_k - 2); jj < issued_k; ++jj)
+        mbar_wait_until(&k_full[jj & 1], (jj >> 1) & 1, deadline);
+      for (int jj = max(0, issued_v - 2); jj < issued_v; ++jj)
+        mbar_wait_until(&v_full[jj & 1], (jj >> 1) & 1, deadline);
     }
   } else {
     // ============================ MMA issuer (warp 5) ============================
@@ -374,22 +437,36 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     bool ok = true;
     if (lane == 0) ok = mbar_wait(q_ready, 0, p.err);
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    for (int j = 0; j < n_tiles && ok && !*abort_flag; ++j) {
+    // S = Q K^T of tile j into S buffer j & 1 (its previous tile's softmax has
+    // finished reading it: the p_full wait of that tile came before)
+    auto issue_qk = [&](int j) -> bool {
       const int s = j & 1;
-      const uint32_t sk = smem_u32(sm + kOffKV + 2 * s * kTile), sv = sk + kTile;
-      if (lane == 0) ok = mbar_wait(&kv_full[s], (j >> 1) & 1, p.err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
+      bool good = true;
+      if (lane == 0) good = mbar_wait(&k_full[s], (j >> 1) & 1, p.err);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (good && lane == 0) {
+        const uint32_t sk = smem_u32(sm + kOffKV + 2 * s * kTile);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kPD / 16; ++ks) {
           const uint32_t koff = (ks >> 2) * (kTile / 2) + (ks & 3) * 32;
-          umma_f16(t_s, umma_desc(sq + koff, 16, 1024), umma_desc(sk + koff, 16, 1024), kIdQK, ks > 0);
+          umma_f16(t_s(j), umma_desc(sq + koff, 16, 1024), umma_desc(sk + koff, 16, 1024), kIdQK, ks > 0);
         }
-        umma_commit(s_full);
-        ok = mbar_wait(p_full, j & 1, p.err);
+        umma_commit(&s_full[s]);
+        umma_commit(&k_empty[s]);
       }
+      __syncwarp();
+      return good;
+    };
+    if (ok && n_tiles > 0) ok = issue_qk(0);
+    for (int j = 0; j < n_tiles && ok && !*abort_flag; ++j) {
+      const int s = j & 1;
+      const uint32_t sv = smem_u32(sm + kOffKV + 2 * s * kTile) + kTile;
+      if (j + 1 < n_tiles && !issue_qk(j + 1)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) ok = mbar_wait(p_full, j & 1, p.err) && mbar_wait(&v_full[s], (j >> 1) & 1, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       // the tile holding the context's last, partial block: its rows past the
@@ -415,7 +492,7 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
                      umma_desc(sv + ks * 2048, kTile / 2, 1024), kIdPV, j > 0 || ks > 0 || pass > 0);
           }
         umma_commit(pv_done);
-        umma_commit(&kv_empty[s]);
+        umma_commit(&v_empty[s]);
       }
       __syncwarp();
     }
@@ -431,7 +508,7 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5)
+  if (warp == 9)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
