@@ -527,6 +527,107 @@ def run_copy(args, rank: int, local_rank: int) -> dict | None:
 
 
 # ---------------------------------------------------------------------------
+# model-wide cache, whole-step graph (--workload layers)
+# ---------------------------------------------------------------------------
+LAYERS_METRIC = "model decode step tokens/s (all layers, one graph launch per step), 1 GPU"
+
+
+def run_layers(args, rank: int, local_rank: int) -> dict | None:
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import paged_kv_cache_153_gb300 as pkv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    li = wl.make_layers()
+    w, L = li.base, li.n_layers
+    t16 = {"f16": torch.float16, "bf16": torch.bfloat16}[w.kv_dtype]
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(t16).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        kc, vc, q, kn, vn = up(li.k_pool), up(li.v_pool), up(li.q), up(li.k_new), up(li.v_new)
+        tables, lens = torch.from_numpy(w.block_tables).to(dev), torch.from_numpy(w.context_lens).to(dev)
+        out = torch.empty_like(q)
+        slots = torch.empty(w.batch, dtype=torch.int64, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        max_ctx = int(w.context_lens.max())
+        ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                                        w.max_blocks_per_seq, max_ctx, 0), dtype=torch.uint8,
+                         device=dev)
+    stream.synchronize()
+    graph = pkv.StepGraph(q, kn, vn, kc, vc, tables, lens, out, scale=w.scale, max_context_len=max_ctx,
+                          workspace=ws, slot_mapping_out=slots, err_flag=err)
+
+    def eager():
+        for l in range(L):
+            pkv.pkv_paged_decode_step_layer(q[l], kn[l], vn[l], kc, vc, tables, lens, out[l], layer=l,
+                                            scale=w.scale, max_context_len=max_ctx, workspace=ws,
+                                            slot_mapping_out=slots, err_flag=err, stream=stream)
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    eager_ms = timed(eager, max(10, min(args.steps, 300)))
+    with ClockSampler(local_rank) as clocks:
+        graph_ms = timed(lambda: graph.launch(stream), args.steps)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())}")
+    # end to end: every layer's queries and new rows from pinned host memory, outputs read back
+    h_q, h_k, h_v = (torch.from_numpy(np.ascontiguousarray(a)).view(t16).pin_memory() for a in (li.q, li.k_new, li.v_new))
+    h_out = torch.empty(out.shape, dtype=t16).pin_memory()
+
+    def host_step():
+        q.copy_(h_q, non_blocking=True)
+        kn.copy_(h_k, non_blocking=True)
+        vn.copy_(h_v, non_blocking=True)
+        graph.launch(stream)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            host_step()
+        n_e2e = max(10, min(args.steps, 1000))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        e2e_s = time.perf_counter() - t0
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    algo = L * (w.algorithmic_bytes() + 2 * w.batch * w.n_kv_heads * w.head_dim * w.kv_elt_bytes)
+    achieved = algo / (graph_ms * 1e-3) / 1e9
+    return {
+        "metric": LAYERS_METRIC, "value": w.batch * 1e3 / graph_ms, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+        "config": {"workload": f"layers: the tiny shape (batch {w.batch}, {w.n_q_heads}/{w.n_kv_heads} heads, head_dim "
+                               f"{w.head_dim}, {w.kv_dtype}) through {L} layers of a [num_blocks, {L}, H_kv, 16, d] "
+                               "cache: every layer's fused decode step, one graph launch per model step",
+                   "num_layers": L, "batch": w.batch, "eager_ms_per_step": eager_ms,
+                   "eager": f"{L} pkv_paged_decode_step_layer calls from Python per step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": f"pkv_step_graph_launch ({2 * L} launches: decode + combine per layer), "
+                     "average over the timed region", "algorithmic_bytes_per_launch": algo,
+                     "avg_launch_ms": graph_ms, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "note": "launch-bound: the bytes per layer are ~0.6 MB"},
+        "gpu_launches": 2 * L * args.steps, "clocks": clocks.summary(),
+        "e2e": {"value": w.batch * n_e2e / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(sum(x.numel() * 2 for x in (h_q, h_k, h_v))),
+                "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": n_e2e,
+                "path": "per-layer queries and new rows from pinned host memory, one graph launch, outputs read back"},
+    }
+
+
+# ---------------------------------------------------------------------------
 # paged prefill / extend attention (--workload prefill)
 # ---------------------------------------------------------------------------
 PREFILL_METRIC = "paged prefill (causal extend attention) TFLOP/s, 1 GPU"
@@ -654,7 +755,7 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow", "prefill"])
+    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow", "prefill", "layers"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -662,6 +763,34 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == "layers":
+        if args.impl == "reference":
+            if rank != 0:
+                return
+            li = wl.make_layers()
+            w = li.base
+            t0, n = time.perf_counter(), 0
+            while time.perf_counter() - t0 < max(1.0, 0.01 * args.steps):
+                oracle_step(w, [n % w.batch])
+                n += 1
+            el = time.perf_counter() - t0
+            rate = n / li.n_layers / el            # one token through every layer
+            print(json.dumps({
+                "impl": "reference", "metric": LAYERS_METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.batch / rate * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": "layers (oracle: one layer step per sequence, "
+                                                            f"x {li.n_layers} layers)"},
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{n} single-sequence layer steps, {el:.1f} s, one host thread"},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+            return
+        res = run_layers(args, rank, local_rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
 
     if args.workload == "prefill":
         pi = wl.make_prefill()

@@ -259,6 +259,48 @@ pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void
                                 size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Multi-layer cache and whole-step launch ("What a KV cache is ...", section
+ * 2.2: one preallocated cache of shape (num_blocks, num_layers, H_kv,
+ * block_size, head_dim) for the whole model, so one block id addresses a token
+ * range in every layer).  k_cache / v_cache are [num_blocks, num_layers,
+ * num_kv_heads, 16, head_dim] (16-bit, 16-byte aligned); block tables and
+ * lengths are shared by all layers.
+ *
+ * pkv_paged_decode_step_layer: pkv_paged_decode_step on layer `layer` of such a
+ * cache (0 <= layer < num_layers; PKV_ERR_INVALID_ARG otherwise).
+ *
+ * pkv_step_graph_create: capture one decode step over all num_layers layers --
+ * for each layer l the fused step with q + l * batch * num_q_heads * head_dim,
+ * k_new / v_new + l * batch * num_kv_heads * head_dim and out + l * batch *
+ * num_q_heads * head_dim elements (q, out [num_layers, batch, Hq, D]; k_new,
+ * v_new [num_layers, batch, Hkv, D]), one workspace reused layer after layer --
+ * into a CUDA graph.  The graph holds these pointers: later launches read
+ * whatever the buffers hold then.  pkv_step_graph_launch replays it on
+ * `stream` (one host call per model step); pkv_step_graph_destroy frees it.
+ * Errors: PKV_ERR_INVALID_ARG for a null handle or bad sizes, PKV_ERR_CUDA if
+ * capture or instantiation fails (pkv_last_error names the call).
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_step_layer(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                       void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                       int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                       int max_blocks_per_seq, int64_t num_blocks, int num_layers, int layer,
+                                       int max_context_len, float scale, void* out, pkv_dtype dtype,
+                                       int partition_tokens, int64_t* slot_mapping_out, void* workspace,
+                                       size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+typedef struct pkv_step_graph pkv_step_graph;
+
+pkv_status pkv_step_graph_create(pkv_step_graph** graph, const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                 int num_layers, int max_context_len, float scale, void* out, pkv_dtype dtype,
+                                 int partition_tokens, int64_t* slot_mapping_out, void* workspace,
+                                 size_t workspace_bytes, int32_t* err_flag);
+pkv_status pkv_step_graph_launch(pkv_step_graph* graph, void* stream);
+void pkv_step_graph_destroy(pkv_step_graph* graph);
+
+/* ---------------------------------------------------------------------------
  * Paged prefill / extend attention ("KV Cache, the memory notepad ...",
  * sections 二-四: prefill attends over the prompt; "Series 03 ...", section 3.1:
  * K/V through the block table, section 5.1: chunked prefill).  The new tokens

@@ -105,3 +105,12 @@ def dequantize_cache(codes_values: np.ndarray, head_scales) -> np.ndarray:
     compute).  The caller decodes the codes with ``oracle.e4m3.decode``."""
     scales = np.asarray(head_scales, dtype=np.float64).reshape(1, -1, 1, 1)
     return codes_values * scales
+
+
+def layer_view(cache: np.ndarray, layer: int) -> np.ndarray:
+    """Layer ``layer`` of a model-wide cache [num_blocks, num_layers, H_kv,
+    block_size, d] ("What a KV cache is ..." section 2.2: one preallocated
+    cache laid out as (num_blocks, num_layers, num_kv_heads, block_size,
+    head_dim), so one block id covers a token range in every layer): the
+    [num_blocks, H_kv, block_size, d] cache that layer's attention reads."""
+    return cache[:, layer]

@@ -22,7 +22,8 @@ __all__ = [
     "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8", "pkv_decode_step_host",
     "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_step", "pkv_paged_decode_step_fp8",
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
-    "pkv_copy_blocks", "pkv_prepare_append", "pkv_paged_prefill_attention",
+    "pkv_copy_blocks", "pkv_prepare_append", "pkv_paged_prefill_attention", "pkv_paged_decode_step_layer",
+    "StepGraph",
 ]
 
 PKV_F16 = 0
@@ -69,6 +70,12 @@ _SIGS = {
     "pkv_copy_blocks": (_i, [_p, _p, _i64, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
     "pkv_paged_prefill_attention": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
                                          _p, _p]),
+    "pkv_paged_decode_step_layer": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _i, _i, _f,
+                                         _p, _i, _i, _p, _p, _sz, _p, _p]),
+    "pkv_step_graph_create": (_i, [C.POINTER(_p), _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
+                                   _i, _f, _p, _i, _i, _p, _p, _sz, _p]),
+    "pkv_step_graph_launch": (_i, [_p, _p]),
+    "pkv_step_graph_destroy": (None, [_p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -270,6 +277,49 @@ def pkv_paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(cu_seqlens),
         context_lens.numel(), q.shape[1], hkv, d, bs, block_tables.shape[1], nb, max_query_len, scale, _ptr(out),
         _dtype_code(q, dtype), _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_step_layer(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, *, layer: int,
+                                scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                                slot_mapping_out=None, dtype=None, err_flag=None, stream=None) -> None:
+    """The fused decode step on layer ``layer`` of a layer-major cache
+    [NB, L, Hkv, 16, D]."""
+    nb, n_layers, hkv, bs, d = k_cache.shape
+    _check("pkv_paged_decode_step_layer", lib.pkv_paged_decode_step_layer(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        q.shape[0], q.shape[1], hkv, d, bs, block_tables.shape[1], nb, n_layers, layer, max_context_len, scale,
+        _ptr(out), _dtype_code(q, dtype), partition_tokens, _ptr(slot_mapping_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
+
+
+class StepGraph:
+    """One decode step over every layer of a layer-major cache, captured into
+    a CUDA graph by the library (pkv_step_graph_*): q, out [L, B, Hq, D];
+    k_new, v_new [L, B, Hkv, D]; caches [NB, L, Hkv, 16, D].  The tensors must
+    outlive the graph; ``launch`` replays the step with their current data."""
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, *, scale: float,
+                 max_context_len: int, workspace, partition_tokens: int = 0, slot_mapping_out=None, dtype=None,
+                 err_flag=None):
+        nb, n_layers, hkv, bs, d = k_cache.shape
+        h = _p()
+        self._keep = (q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, workspace,
+                      slot_mapping_out, err_flag)
+        _check("pkv_step_graph_create", lib.pkv_step_graph_create(
+            C.byref(h), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), q.shape[1], q.shape[2], hkv, d, bs, block_tables.shape[1], nb, n_layers,
+            max_context_len, scale, _ptr(out), _dtype_code(q, dtype), partition_tokens, _ptr(slot_mapping_out),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_flag)))
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        _check("pkv_step_graph_launch", lib.pkv_step_graph_launch(self._h, _stream(stream)))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib.pkv_step_graph_destroy(h)
+            self._h = None
 
 
 def pkv_blocks_needed(num_tokens: int, block_size: int = 16) -> int:

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <mutex>
+#include <new>
 
 #include "decode_launch.cuh"
 #include "host_util.h"
@@ -122,7 +123,7 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
                          int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale, void* out,
                          pkv_dtype dtype, int partition_tokens, void* workspace, size_t workspace_bytes,
                          int32_t* err_flag, void* stream, const void* k_new = nullptr, const void* v_new = nullptr,
-                         int64_t* slots_out = nullptr) {
+                         int64_t* slots_out = nullptr, int num_layers = 1, int layer = 0) {
   if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks < 0 ||
       max_context_len < 0 || partition_tokens < 0 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
@@ -132,6 +133,7 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   const int group = n_q_heads / n_kv_heads;
   if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
   if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+  if (num_layers < 1 || layer < 0 || layer >= num_layers) return PKV_ERR_INVALID_ARG;
   if (batch == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
     return PKV_ERR_INVALID_ARG;
@@ -157,10 +159,16 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   char* ws = static_cast<char*>(workspace);
   DecodeParams p{};
   p.q = q;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.k_scale = fp8 ? k_scale : nullptr;
-  p.v_scale = fp8 ? v_scale : nullptr;
+  // A layer-major cache [num_blocks, num_layers, H_kv, 16, d]: this layer's
+  // view starts layer * H_kv slabs into block 0, and blocks are num_layers *
+  // H_kv slabs apart (per-layer scales [num_layers, H_kv]).
+  const int64_t slab_bytes = static_cast<int64_t>(kBlockSize) * head_dim * (fp8 ? 1 : 2);
+  const int64_t layer_off = static_cast<int64_t>(layer) * n_kv_heads * slab_bytes;
+  p.k_cache = k_cache ? static_cast<const char*>(k_cache) + layer_off : nullptr;
+  p.v_cache = v_cache ? static_cast<const char*>(v_cache) + layer_off : nullptr;
+  p.k_scale = fp8 ? k_scale + static_cast<int64_t>(layer) * n_kv_heads : nullptr;
+  p.v_scale = fp8 ? v_scale + static_cast<int64_t>(layer) * n_kv_heads : nullptr;
+  p.block_heads = num_layers * n_kv_heads;
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
@@ -265,6 +273,88 @@ extern "C" pkv_status pkv_paged_decode_step(const void* q, const void* k_new, co
                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
                        max_context_len, scale, out, dtype, partition_tokens, workspace, workspace_bytes, err_flag,
                        stream, k_new, v_new, slot_mapping_out);
+}
+
+extern "C" pkv_status pkv_paged_decode_step_layer(const void* q, const void* k_new, const void* v_new,
+                                                  void* k_cache, void* v_cache, const int32_t* block_tables,
+                                                  const int32_t* context_lens, int batch, int num_q_heads,
+                                                  int num_kv_heads, int head_dim, int block_size,
+                                                  int max_blocks_per_seq, int64_t num_blocks, int num_layers,
+                                                  int layer, int max_context_len, float scale, void* out,
+                                                  pkv_dtype dtype, int partition_tokens, int64_t* slot_mapping_out,
+                                                  void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                  void* stream) {
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  return decode_common(false, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       max_context_len, scale, out, dtype, partition_tokens, workspace, workspace_bytes, err_flag,
+                       stream, k_new, v_new, slot_mapping_out, num_layers, layer);
+}
+
+// One decode step over every layer of a layer-major cache, captured once into
+// a CUDA graph and replayed with one launch.
+struct pkv_step_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" void pkv_step_graph_destroy(pkv_step_graph* g) {
+  if (g == nullptr) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
+extern "C" pkv_status pkv_step_graph_create(pkv_step_graph** out_graph, const void* q, const void* k_new,
+                                            const void* v_new, void* k_cache, void* v_cache,
+                                            const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                            int max_blocks_per_seq, int64_t num_blocks, int num_layers,
+                                            int max_context_len, float scale, void* out, pkv_dtype dtype,
+                                            int partition_tokens, int64_t* slot_mapping_out, void* workspace,
+                                            size_t workspace_bytes, int32_t* err_flag) {
+  if (out_graph == nullptr || num_layers < 1 || batch <= 0 || !q || !k_new || !v_new || !out)
+    return PKV_ERR_INVALID_ARG;
+  *out_graph = nullptr;
+  const int64_t q_layer = static_cast<int64_t>(batch) * num_q_heads * head_dim * 2;
+  const int64_t kv_layer = static_cast<int64_t>(batch) * num_kv_heads * head_dim * 2;
+  cudaStream_t cs = nullptr;
+  if (cuda_failed(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking), "cudaStreamCreateWithFlags"))
+    return PKV_ERR_CUDA;
+  pkv_step_graph* g = new (std::nothrow) pkv_step_graph;
+  if (g == nullptr) {
+    cudaStreamDestroy(cs);
+    return PKV_ERR_CUDA;
+  }
+  pkv_status st = PKV_OK;
+  if (cuda_failed(cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed), "cudaStreamBeginCapture")) {
+    st = PKV_ERR_CUDA;
+  } else {
+    for (int l = 0; l < num_layers && st == PKV_OK; ++l)
+      st = decode_common(false, static_cast<const char*>(q) + l * q_layer, k_cache, v_cache, nullptr, nullptr,
+                         block_tables, context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq, num_blocks, max_context_len, scale, static_cast<char*>(out) + l * q_layer,
+                         dtype, partition_tokens, workspace, workspace_bytes, err_flag, cs,
+                         static_cast<const char*>(k_new) + l * kv_layer, static_cast<const char*>(v_new) + l * kv_layer,
+                         slot_mapping_out, num_layers, l);
+    const cudaError_t e = cudaStreamEndCapture(cs, &g->graph);
+    if (st == PKV_OK && cuda_failed(e, "cudaStreamEndCapture")) st = PKV_ERR_CUDA;
+  }
+  if (st == PKV_OK && cuda_failed(cudaGraphInstantiate(&g->exec, g->graph, 0), "cudaGraphInstantiate"))
+    st = PKV_ERR_CUDA;
+  cudaStreamDestroy(cs);
+  if (st != PKV_OK) {
+    pkv_step_graph_destroy(g);
+    return st;
+  }
+  *out_graph = g;
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_step_graph_launch(pkv_step_graph* g, void* stream) {
+  if (g == nullptr || g->exec == nullptr) return PKV_ERR_INVALID_ARG;
+  return cuda_failed(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)), "cudaGraphLaunch") ? PKV_ERR_CUDA
+                                                                                                     : PKV_OK;
 }
 
 extern "C" pkv_status pkv_paged_decode_step_fp8(const void* q, const void* k_new, const void* v_new,

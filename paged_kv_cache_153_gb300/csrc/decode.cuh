@@ -85,6 +85,9 @@ struct DecodeParams {
   int batch;
   int n_q_heads;
   int n_kv_heads;
+  int block_heads;               // (block, head) slabs per cache block: n_kv_heads, or
+                                 // num_layers * n_kv_heads for a layer-major cache whose
+                                 // base points at this layer
   int max_blocks_per_seq;
   int max_nblk;                  // ceil(max_context_len / 16)
   int part_blocks;               // 0 = balanced ranges
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         if (reports) p.slots_out[b] = -1;
         continue;
       }
-      const int64_t row = (static_cast<int64_t>(blk) * Hkv + g) * kBlockSize + pos % kBlockSize;
+      const int64_t row = (static_cast<int64_t>(blk) * p.block_heads + g) * kBlockSize + pos % kBlockSize;
       if (reports) p.slots_out[b] = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
       unsigned char* dst =
           static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache)) + (row * D + 8 * c) * T::kEsz;
@@ -604,7 +607,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             if (ok) {
               mbar_arrive_expect_tx(&full_bar[s], T::kStage);
               if constexpr (MMA) {
-                const int y = (ids * Hkv + g) * kBlockSize;
+                const int y = (ids * p.block_heads + g) * kBlockSize;
 #pragma unroll
                 for (int t = 0; t < T::kSubTiles; ++t) {
                   tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                               pol_stream);
                 }
               } else {
-                const int64_t slab = (static_cast<int64_t>(ids) * Hkv + g) * T::kSlab;
+                const int64_t slab = (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab;
                 bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
                 bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
               }

@@ -104,7 +104,8 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   li.grid = grid;
   li.stages = stages;
   if constexpr (MMA) {
-    const int64_t rows = p.num_blocks * p.n_kv_heads * kBlockSize;
+    // rows from this layer's base to the end of its last block's slabs
+    const int64_t rows = ((p.num_blocks - 1) * p.block_heads + p.n_kv_heads) * kBlockSize;
     if (rows > INT32_MAX) return PKV_ERR_UNSUPPORTED;    // TMA row coordinates are 32-bit
     if (!encode_cache_tmap(&p.tmap_k, p.k_cache, rows, D, Tr::kEsz) ||
         !encode_cache_tmap(&p.tmap_v, p.v_cache, rows, D, Tr::kEsz))

@@ -24,6 +24,10 @@ planning article):
               per-KV-head scales; batch 32: 29 contexts of 2048 and 3 of 65536
               (positions drawn from the seed); partitions of 512 tokens.
 
+Model-wide cache inputs (``layers_inputs``, ``make_layers``): random pools of
+shape [num_blocks, num_layers, H_kv, 16, d] and per-layer queries / new rows
+over one workload's tables.
+
 Prefill inputs (``prefill_inputs``, ``make_prefill``): sequences with a
 cached prefix and new tokens after it, random queries and pool, tables from a
 random permutation of the pool.
@@ -400,6 +404,43 @@ def make_prefill(seed: int = 1300) -> PrefillInputs:
     each; Llama-3-8B-like heads (32 query / 8 KV, d 128, bf16)."""
     return prefill_inputs("prefill", cached_lens=[2048] * 4, new_lens=[2048] * 4, n_q_heads=32, n_kv_heads=8,
                           head_dim=128, dtype="bf16", seed=seed)
+
+
+# ----------------------------------------------------------------------------
+# model-wide (layer-major) cache inputs
+# ----------------------------------------------------------------------------
+@dataclass
+class LayerInputs:
+    """One decode step of an ``n_layers``-layer model over a cache laid out
+    [num_blocks, n_layers, H_kv, 16, d]: ``base`` carries the shapes, tables,
+    lengths and scale shared by all layers; every layer has its own pool
+    slice, queries and new rows."""
+    base: Workload
+    n_layers: int
+    k_pool: np.ndarray             # [NB, L, Hkv, 16, d] 16-bit bits
+    v_pool: np.ndarray
+    q: np.ndarray                  # [L, B, Hq, d]
+    k_new: np.ndarray              # [L, B, Hkv, d]
+    v_new: np.ndarray
+
+
+def layers_inputs(base: Workload, n_layers: int, seed: int) -> LayerInputs:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    w = base
+    nb, L = w.num_blocks, n_layers
+    return LayerInputs(
+        base=w, n_layers=L,
+        k_pool=_normal_bits(rng, (nb, L, w.n_kv_heads, BLOCK_SIZE, w.head_dim), w.kv_dtype),
+        v_pool=_normal_bits(rng, (nb, L, w.n_kv_heads, BLOCK_SIZE, w.head_dim), w.kv_dtype),
+        q=_normal_bits(rng, (L, w.batch, w.n_q_heads, w.head_dim), w.dtype),
+        k_new=_normal_bits(rng, (L, w.batch, w.n_kv_heads, w.head_dim), w.kv_dtype),
+        v_new=_normal_bits(rng, (L, w.batch, w.n_kv_heads, w.head_dim), w.kv_dtype))
+
+
+def make_layers(seed: int = 1400) -> LayerInputs:
+    """The tiny workload's shape (batch 4, 4 = 4 heads, d 64, fp16, contexts
+    U{1..256}) through 32 layers: a step whose calls are launch-bound."""
+    return layers_inputs(make("tiny"), 32, seed)
 
 
 def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
