@@ -527,6 +527,87 @@ def run_copy(args, rank: int, local_rank: int) -> dict | None:
 
 
 # ---------------------------------------------------------------------------
+# INT8 per-block min-max cache (--workload int8)
+# ---------------------------------------------------------------------------
+INT8_METRIC = "INT8-KV decode step tokens/s and achieved HBM GB/s, 1 GPU"
+
+
+def int8_bytes(w) -> int:
+    """KV codes (1 byte per element) + the 16-byte scalars of every (block,
+    head) slab read + q + out."""
+    nblk = sum(-(-int(n) // 16) for n in w.context_lens)
+    return nblk * w.n_kv_heads * (2 * 16 * w.head_dim + 16) + 2 * w.batch * w.n_q_heads * w.head_dim * 2
+
+
+def run_int8(args, rank: int, local_rank: int) -> dict | None:
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import paged_kv_cache_153_gb300 as pkv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = wl.make("gqa8b")
+    bf = torch.bfloat16
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(bf).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        kc = torch.empty(w.k_pool.shape, dtype=torch.uint8, device=dev)
+        vc = torch.empty_like(kc)
+        prm = torch.empty(w.num_blocks, w.n_kv_heads, 4, dtype=torch.float32, device=dev)
+        pkv.pkv_kv_quantize_int8(up(w.k_pool), up(w.v_pool), kc, vc, prm, stream=stream)
+        q, kn, vn = up(w.q), up(w.k_new), up(w.v_new)
+        tables, lens = torch.from_numpy(w.block_tables).to(dev), torch.from_numpy(w.context_lens).to(dev)
+        slots = torch.empty(w.batch, dtype=torch.int64, device=dev)
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        max_ctx = int(w.context_lens.max())
+        ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                                        w.max_blocks_per_seq, max_ctx, 0), dtype=torch.uint8,
+                         device=dev)
+    stream.synchronize()
+
+    def step():
+        pkv.pkv_slot_mapping(tables, lens, slots, num_blocks=w.num_blocks, position_offset=-1, err_flag=err,
+                             stream=stream)
+        pkv.pkv_kv_append_int8(kn, vn, slots, kc, vc, prm, err_flag=err, stream=stream)
+        pkv.pkv_paged_decode_attention_int8(q, kc, vc, prm, tables, lens, out, scale=w.scale, max_context_len=max_ctx,
+                                            workspace=ws, err_flag=err, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+    per_ms = a.elapsed_time(b) / args.steps
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())}")
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    algo = int8_bytes(w)
+    achieved = algo / (per_ms * 1e-3) / 1e9
+    return {
+        "metric": INT8_METRIC, "value": w.batch * 1e3 / per_ms, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": dict(describe(w), workload=f"int8: the gqa8b shape with the KV cache as INT8 codes + per-(block, "
+                       "head) min-max scalars (bf16 q/out)", step="slot mapping + INT8 append (re-quantising the "
+                       "block) + INT8 paged decode attention (decode + combine)"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "the step's four launches, average over the timed region",
+                     "algorithmic_bytes_per_launch": algo, "avg_launch_ms": per_ms,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth"},
+        "gpu_launches": 4 * args.steps, "clocks": clocks.summary(), "e2e": None,
+    }
+
+
+# ---------------------------------------------------------------------------
 # model-wide cache, whole-step graph (--workload layers)
 # ---------------------------------------------------------------------------
 LAYERS_METRIC = "model decode step tokens/s (all layers, one graph launch per step), 1 GPU"
@@ -755,7 +836,7 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow", "prefill", "layers"])
+    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow", "prefill", "layers", "int8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -763,6 +844,16 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == "int8":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the int8 bench line has no reference arm; "
+                              "its parity is in tests/test_gpu_int8.py"}), flush=True)
+            return
+        res = run_int8(args, rank, local_rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
 
     if args.workload == "layers":
         if args.impl == "reference":

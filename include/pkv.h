@@ -259,6 +259,47 @@ pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void
                                 size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * INT8 KV cache with per-block min-max scaling ("What a KV cache is ...",
+ * section 3.3: q = round((k - k_min) / (k_max - k_min) * 255), two scalars
+ * per block).  Codes are uint8 [num_blocks, num_kv_heads, 16, head_dim]; the
+ * scalars are per (block, KV head) for K and for V, stored as float
+ * [num_blocks, num_kv_heads, 4] = (k_min, k_max, v_min, v_max) (16-byte
+ * aligned).  Encoding: float32 in the formula's order with IEEE rounding,
+ * round half to even, clamped to [0, 255]; max == min gives 0; rows of a
+ * block that hold no token have code 0 and do not enter min / max.
+ * Decoding: x = min + q (max - min) / 255.
+ *
+ * pkv_kv_quantize_int8: quantise 16-bit pools k_src / v_src [num_blocks,
+ * num_kv_heads, 16, head_dim] of src_dtype; rows_used (device int32
+ * [num_blocks], nullable = 16 each) gives the rows of each block that hold
+ * tokens.
+ * pkv_kv_append_int8: write token t's rows k_new / v_new [T, num_kv_heads,
+ * head_dim] (in_dtype) at slot_mapping[t] (< 0 skips; past the pool:
+ * PKV_ERR_OOB) and re-quantise rows 0..slot % 16 of that block: the old codes
+ * are decoded in float32 as min + ((q * (max - min)) / 255), min / max are
+ * taken again over those rows and the new one, and all of them are encoded
+ * again.  The tokens of one call must lie in distinct blocks.
+ * pkv_paged_decode_attention_int8: pkv_paged_decode_attention over such a
+ * cache; dequantisation happens in registers as k_min sum(q) + dk (q . codes)
+ * per score and v_min sum(p) + dv (p . codes) per output.  q_dtype is the type
+ * of q and out.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_kv_quantize_int8(const void* k_src, const void* v_src, uint8_t* k_cache, uint8_t* v_cache,
+                                float* slab_params, const int32_t* rows_used, int64_t num_blocks, int num_kv_heads,
+                                int head_dim, int block_size, pkv_dtype src_dtype, int32_t* err_flag, void* stream);
+pkv_status pkv_kv_append_int8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t num_tokens,
+                              uint8_t* k_cache, uint8_t* v_cache, float* slab_params, int64_t num_blocks,
+                              int num_kv_heads, int head_dim, int block_size, pkv_dtype in_dtype, int32_t* err_flag,
+                              void* stream);
+pkv_status pkv_paged_decode_attention_int8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                           const float* slab_params, const int32_t* block_tables,
+                                           const int32_t* context_lens, int batch, int num_q_heads, int num_kv_heads,
+                                           int head_dim, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                           int max_context_len, float scale, void* out, pkv_dtype q_dtype,
+                                           int partition_tokens, void* workspace, size_t workspace_bytes,
+                                           int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Multi-layer cache and whole-step launch ("What a KV cache is ...", section
  * 2.2: one preallocated cache of shape (num_blocks, num_layers, H_kv,
  * block_size, head_dim) for the whole model, so one block id addresses a token

@@ -23,7 +23,7 @@ __all__ = [
     "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_step", "pkv_paged_decode_step_fp8",
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
     "pkv_copy_blocks", "pkv_prepare_append", "pkv_paged_prefill_attention", "pkv_paged_decode_step_layer",
-    "StepGraph",
+    "StepGraph", "pkv_kv_quantize_int8", "pkv_kv_append_int8", "pkv_paged_decode_attention_int8",
 ]
 
 PKV_F16 = 0
@@ -76,6 +76,10 @@ _SIGS = {
                                    _i, _f, _p, _i, _i, _p, _p, _sz, _p]),
     "pkv_step_graph_launch": (_i, [_p, _p]),
     "pkv_step_graph_destroy": (None, [_p]),
+    "pkv_kv_quantize_int8": (_i, [_p, _p, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
+    "pkv_kv_append_int8": (_i, [_p, _p, _p, _i64, _p, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
+    "pkv_paged_decode_attention_int8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
+                                             _i, _p, _sz, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -320,6 +324,34 @@ class StepGraph:
         if h:
             lib.pkv_step_graph_destroy(h)
             self._h = None
+
+
+def pkv_kv_quantize_int8(k_src, v_src, k_cache, v_cache, slab_params, *, rows_used=None, dtype=None,
+                         err_flag=None, stream=None) -> None:
+    """INT8 codes and per-(block, head) (k_min, k_max, v_min, v_max) of 16-bit pools."""
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_kv_quantize_int8", lib.pkv_kv_quantize_int8(
+        _ptr(k_src), _ptr(v_src), _ptr(k_cache), _ptr(v_cache), _ptr(slab_params), _ptr(rows_used), nb, hkv, d, bs,
+        _dtype_code(k_src, dtype), _ptr(err_flag), _stream(stream)))
+
+
+def pkv_kv_append_int8(k_new, v_new, slot_mapping, k_cache, v_cache, slab_params, *, dtype=None, err_flag=None,
+                       stream=None) -> None:
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_kv_append_int8", lib.pkv_kv_append_int8(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), slot_mapping.numel(), _ptr(k_cache), _ptr(v_cache),
+        _ptr(slab_params), nb, hkv, d, bs, _dtype_code(k_new, dtype), _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_attention_int8(q, k_cache, v_cache, slab_params, block_tables, context_lens, out, *,
+                                    scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                                    q_dtype=None, err_flag=None, stream=None) -> None:
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_paged_decode_attention_int8", lib.pkv_paged_decode_attention_int8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(slab_params), _ptr(block_tables), _ptr(context_lens),
+        q.shape[0], q.shape[1], hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale, _ptr(out),
+        _dtype_code(q, q_dtype), partition_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(err_flag), _stream(stream)))
 
 
 def pkv_blocks_needed(num_tokens: int, block_size: int = 16) -> int:

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpkv.so")
 
 CUDA_SOURCES = ["append.cu", "api.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "noalloc.cu",
-                "prefill.cu"]
+                "prefill.cu", "decode_int8.cu", "append_int8.cu"]
 CXX_SOURCES = ["pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

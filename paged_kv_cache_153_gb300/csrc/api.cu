@@ -117,13 +117,17 @@ bool ws_layout(int batch, int n_kv_heads, int group, int head_dim, int max_block
   return true;
 }
 
-pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                          const float* v_scale, const int32_t* block_tables, const int32_t* context_lens,
                          int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale, void* out,
                          pkv_dtype dtype, int partition_tokens, void* workspace, size_t workspace_bytes,
                          int32_t* err_flag, void* stream, const void* k_new = nullptr, const void* v_new = nullptr,
-                         int64_t* slots_out = nullptr, int num_layers = 1, int layer = 0) {
+                         int64_t* slots_out = nullptr, int num_layers = 1, int layer = 0,
+                         const void* slab_params = nullptr) {
+  // kv_kind: 0 = 16-bit cache, 1 = E4M3 with per-head scales, 2 = INT8 with
+  // per-(block, head) min-max parameters
+  const bool fp8 = kv_kind == 1, int8 = kv_kind == 2;
   if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks < 0 ||
       max_context_len < 0 || partition_tokens < 0 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
@@ -151,7 +155,10 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   if (workspace_bytes < w.total) return PKV_ERR_WORKSPACE;
   if (w.slots > INT32_MAX) return PKV_ERR_UNSUPPORTED;
 
-  DecodeLauncher launch = fp8 ? decode_launcher_e4m3(dtype, head_dim, group)
+  if (int8 && (!slab_params || (reinterpret_cast<uintptr_t>(slab_params) & 15u) || k_new != nullptr))
+    return PKV_ERR_INVALID_ARG;
+  DecodeLauncher launch = int8 ? decode_launcher_int8(dtype, head_dim, group)
+                        : fp8 ? decode_launcher_e4m3(dtype, head_dim, group)
                               : (dtype == PKV_F16 ? decode_launcher_f16(head_dim, group)
                                                   : decode_launcher_bf16(head_dim, group));
   if (launch == nullptr) return PKV_ERR_UNSUPPORTED;
@@ -162,13 +169,15 @@ pkv_status decode_common(bool fp8, const void* q, const void* k_cache, const voi
   // A layer-major cache [num_blocks, num_layers, H_kv, 16, d]: this layer's
   // view starts layer * H_kv slabs into block 0, and blocks are num_layers *
   // H_kv slabs apart (per-layer scales [num_layers, H_kv]).
-  const int64_t slab_bytes = static_cast<int64_t>(kBlockSize) * head_dim * (fp8 ? 1 : 2);
+  const int64_t slab_bytes = static_cast<int64_t>(kBlockSize) * head_dim * (kv_kind ? 1 : 2);
   const int64_t layer_off = static_cast<int64_t>(layer) * n_kv_heads * slab_bytes;
   p.k_cache = k_cache ? static_cast<const char*>(k_cache) + layer_off : nullptr;
   p.v_cache = v_cache ? static_cast<const char*>(v_cache) + layer_off : nullptr;
   p.k_scale = fp8 ? k_scale + static_cast<int64_t>(layer) * n_kv_heads : nullptr;
   p.v_scale = fp8 ? v_scale + static_cast<int64_t>(layer) * n_kv_heads : nullptr;
   p.block_heads = num_layers * n_kv_heads;
+  p.slab_params = int8 ? static_cast<const float4*>(slab_params) + static_cast<int64_t>(layer) * n_kv_heads
+                       : nullptr;
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
@@ -273,6 +282,20 @@ extern "C" pkv_status pkv_paged_decode_step(const void* q, const void* k_new, co
                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
                        max_context_len, scale, out, dtype, partition_tokens, workspace, workspace_bytes, err_flag,
                        stream, k_new, v_new, slot_mapping_out);
+}
+
+extern "C" pkv_status pkv_paged_decode_attention_int8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                                      const float* slab_params, const int32_t* block_tables,
+                                                      const int32_t* context_lens, int batch, int num_q_heads,
+                                                      int num_kv_heads, int head_dim, int block_size,
+                                                      int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                                      float scale, void* out, pkv_dtype q_dtype, int partition_tokens,
+                                                      void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                      void* stream) {
+  return decode_common(2, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_context_len, scale,
+                       out, q_dtype, partition_tokens, workspace, workspace_bytes, err_flag, stream, nullptr, nullptr,
+                       nullptr, 1, 0, slab_params);
 }
 
 extern "C" pkv_status pkv_paged_decode_step_layer(const void* q, const void* k_new, const void* v_new,

@@ -1,0 +1,199 @@
+// INT8 KV cache with per-block min-max scaling ("What a KV cache is and why it
+// is the crux of LLM inference", section 3.3):
+//   q = round((x - min) / (max - min) * 255)
+// with (min, max) per (block, KV head) for K and for V, kept as float4
+// (k_min, k_max, v_min, v_max) per slab.  Arithmetic is float32 in the
+// formula's order with IEEE rounding (no contraction), round half to even,
+// clamped to [0, 255]; max == min gives 0.  Rows past the ones holding tokens
+// have code 0.  Appending a token re-quantises its block's rows so far: the
+// old codes are decoded as min + ((q * (max - min)) / 255), the new row added,
+// min / max taken again and every row encoded again.
+#include <cuda_runtime.h>
+
+#include "host_util.h"
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+constexpr int kQThreads = 256;
+constexpr int kQPer = 8;   // values per thread: 16 rows x 128 / 256
+
+__device__ __forceinline__ uint8_t int8_code(float x, float lo, float span) {
+  if (span == 0.f) return 0;
+  const float t = __fmul_rn(__fdiv_rn(__fsub_rn(x, lo), span), 255.f);
+  return static_cast<uint8_t>(fminf(fmaxf(rintf(t), 0.f), 255.f));
+}
+
+__device__ __forceinline__ float int8_decode_f32(uint8_t q, float lo, float hi) {
+  const float span = __fsub_rn(hi, lo);
+  return __fadd_rn(lo, __fdiv_rn(__fmul_rn(static_cast<float>(q), span), 255.f));
+}
+
+// block-wide min and max of one value per thread (NaN-free inputs)
+__device__ __forceinline__ float2 block_minmax(float lo, float hi, float2* scratch) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, m));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, m));
+  }
+  const int warp = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) scratch[warp] = make_float2(lo, hi);
+  __syncthreads();
+  float2 r = scratch[0];
+  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) {
+    r.x = fminf(r.x, scratch[w].x);
+    r.y = fmaxf(r.y, scratch[w].y);
+  }
+  return r;
+}
+
+template <typename IN>
+__device__ __forceinline__ float in_f32(const void* base, int64_t i, IN);
+template <>
+__device__ __forceinline__ float in_f32(const void* base, int64_t i, F16) {
+  return __half2float(static_cast<const __half*>(base)[i]);
+}
+template <>
+__device__ __forceinline__ float in_f32(const void* base, int64_t i, BF16) {
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+}
+
+// one thread block per (block, KV head): quantise rows [0, n) of the K and V slabs
+template <typename IN>
+__global__ void __launch_bounds__(kQThreads) quantize_int8_kernel(const void* k_src, const void* v_src,
+                                                                  uint8_t* k_codes, uint8_t* v_codes,
+                                                                  float4* params, const int32_t* rows_used,
+                                                                  int n_heads, int d) {
+  __shared__ float2 scratch[kQThreads / 32];
+  pdl_wait_and_release();
+  const int64_t slab = blockIdx.x;             // block * n_heads + head
+  const int blk = static_cast<int>(slab / n_heads);
+  const int n = rows_used ? min(max(rows_used[blk], 0), kBlockSize) : kBlockSize;
+  const int count = n * d;
+  float lohi[4];
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    const void* src = which ? v_src : k_src;
+    uint8_t* dst = (which ? v_codes : k_codes) + slab * kBlockSize * d;
+    float x[kQPer];
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = threadIdx.x + k * kQThreads;
+      x[k] = (i < count) ? in_f32(src, slab * kBlockSize * d + i, IN{}) : 0.f;
+      if (i < count) {
+        lo = fminf(lo, x[k]);
+        hi = fmaxf(hi, x[k]);
+      }
+    }
+    const float2 mm = block_minmax(lo, hi, scratch);
+    const float span = (count > 0) ? __fsub_rn(mm.y, mm.x) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = threadIdx.x + k * kQThreads;
+      if (i < kBlockSize * d) dst[i] = (i < count) ? int8_code(x[k], mm.x, span) : 0;
+    }
+    lohi[2 * which] = count > 0 ? mm.x : 0.f;
+    lohi[2 * which + 1] = count > 0 ? mm.y : 0.f;
+  }
+  if (threadIdx.x == 0) params[slab] = make_float4(lohi[0], lohi[1], lohi[2], lohi[3]);
+}
+
+// one thread block per (token, KV head): write the token's row and re-quantise
+// rows [0, row] of its block's K and V slabs
+template <typename IN>
+__global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_new, const void* v_new,
+                                                                const int64_t* slots, uint8_t* k_codes,
+                                                                uint8_t* v_codes, float4* params,
+                                                                int64_t num_slots, int n_heads, int d,
+                                                                int32_t* err) {
+  __shared__ float2 scratch[kQThreads / 32];
+  pdl_wait_and_release();
+  const int64_t t = blockIdx.x / n_heads;
+  const int h = static_cast<int>(blockIdx.x % n_heads);
+  const int64_t s = slots[t];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (threadIdx.x == 0) record_error(err, PKV_ERR_OOB);
+    return;
+  }
+  const int64_t slab = (s / kBlockSize) * n_heads + h;
+  const int row = static_cast<int>(s % kBlockSize);
+  const int count = (row + 1) * d;
+  float4 prm = params[slab];
+  float out_lohi[4];
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    uint8_t* codes = (which ? v_codes : k_codes) + slab * kBlockSize * d;
+    const float lo_old = which ? prm.z : prm.x, hi_old = which ? prm.w : prm.y;
+    const void* src = which ? v_new : k_new;
+    float x[kQPer];
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = threadIdx.x + k * kQThreads;
+      x[k] = 0.f;
+      if (i < count) {
+        x[k] = (i >= row * d) ? in_f32(src, (t * n_heads + h) * d + (i - row * d), IN{})
+                              : int8_decode_f32(codes[i], lo_old, hi_old);
+        lo = fminf(lo, x[k]);
+        hi = fmaxf(hi, x[k]);
+      }
+    }
+    const float2 mm = block_minmax(lo, hi, scratch);   // (its barriers order every read before the writes)
+    const float span = __fsub_rn(mm.y, mm.x);
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = threadIdx.x + k * kQThreads;
+      if (i < count) codes[i] = int8_code(x[k], mm.x, span);
+    }
+    out_lohi[2 * which] = mm.x;
+    out_lohi[2 * which + 1] = mm.y;
+  }
+  if (threadIdx.x == 0) params[slab] = make_float4(out_lohi[0], out_lohi[1], out_lohi[2], out_lohi[3]);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_kv_quantize_int8(const void* k_src, const void* v_src, uint8_t* k_cache, uint8_t* v_cache,
+                                           float* slab_params, const int32_t* rows_used, int64_t num_blocks,
+                                           int num_kv_heads, int head_dim, int block_size, pkv_dtype src_dtype,
+                                           int32_t* err_flag, void* stream) {
+  (void)err_flag;
+  if (num_blocks < 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (num_blocks == 0) return PKV_OK;
+  if (!k_src || !v_src || !k_cache || !v_cache || !slab_params || (reinterpret_cast<uintptr_t>(slab_params) & 15u))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t slabs = num_blocks * num_kv_heads;
+  if (slabs > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  auto kern = src_dtype == PKV_F16 ? quantize_int8_kernel<F16> : quantize_int8_kernel<BF16>;
+  const cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(slabs)), dim3(kQThreads), 0,
+                                   static_cast<cudaStream_t>(stream), k_src, v_src, k_cache, v_cache,
+                                   reinterpret_cast<float4*>(slab_params), rows_used, num_kv_heads, head_dim);
+  return cuda_failed(e, "quantize_int8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
+}
+
+extern "C" pkv_status pkv_kv_append_int8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                         int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache, float* slab_params,
+                                         int64_t num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                         pkv_dtype in_dtype, int32_t* err_flag, void* stream) {
+  if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (in_dtype != PKV_F16 && in_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !slab_params ||
+      (reinterpret_cast<uintptr_t>(slab_params) & 15u))
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens * num_kv_heads > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  auto kern = in_dtype == PKV_F16 ? append_int8_kernel<F16> : append_int8_kernel<BF16>;
+  const cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(num_tokens * num_kv_heads)), dim3(kQThreads), 0,
+                                   static_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping, k_cache, v_cache,
+                                   reinterpret_cast<float4*>(slab_params), num_blocks * kBlockSize, num_kv_heads,
+                                   head_dim, err_flag);
+  return cuda_failed(e, "append_int8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
+}

@@ -71,6 +71,7 @@ struct DecodeParams {
   const void* v_cache;
   const float* k_scale;          // [Hkv] (E4M3 cache only)
   const float* v_scale;
+  const float4* slab_params;     // INT8 cache: [NB * block_heads] (k_min, k_max, v_min, v_max)
   const int32_t* block_tables;   // [B, max_blocks_per_seq]
   const int32_t* context_lens;   // [B]
   void* out;                     // [B, Hq, D] 16-bit
@@ -169,7 +170,10 @@ template <int D, int G, int NW, typename KV, bool MMA>
 struct DecodeTraits {
   static constexpr int kEsz = KV::kBytes;
   static constexpr int kSlab = kBlockSize * D * kEsz;          // bytes of one (block, head) slab
-  static constexpr int kStage = 2 * kSlab;                     // K + V
+  // INT8 caches stage each block's 16-byte (k_min, k_max, v_min, v_max) after V
+  static constexpr int kParam = std::is_same<KV, U8>::value ? 16 : 0;
+  static constexpr int kStage = 2 * kSlab + (kParam ? 128 : 0);  // K + V (+ params, padded)
+  static constexpr int kTx = 2 * kSlab + kParam;                 // bytes a stage receives
   static constexpr int kSubTiles = (D * kEsz) / 128;           // swizzled [16 x 128 B] tiles per slab
   static constexpr int kQBytes = G * D * 2;
   static constexpr int kThreads = (NW + 1) * 32;
@@ -182,6 +186,7 @@ struct DecodeTraits {
   static_assert(kNF == (G >= 2 ? G / 2 : 1), "lane/head mapping");
   static_assert(!MMA || (G >= 2 && G <= 8 && (D * kEsz) % 128 == 0 && (kEsz == 2 || D * kEsz == 128)),
                 "tensor-core variant");
+  static_assert(!(MMA && kParam), "INT8 caches use the CUDA-core consumer");
 
   // shared memory layout (byte offsets from a 1024-byte aligned base)
   static __host__ __device__ size_t q_off(int stages) { return static_cast<size_t>(stages) * kStage; }
@@ -605,7 +610,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             stage_ok[s] = ok ? 1 : 0;
             unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
             if (ok) {
-              mbar_arrive_expect_tx(&full_bar[s], T::kStage);
+              mbar_arrive_expect_tx(&full_bar[s], T::kTx);
               if constexpr (MMA) {
                 const int y = (ids * p.block_heads + g) * kBlockSize;
 #pragma unroll
@@ -618,6 +623,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                 const int64_t slab = (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab;
                 bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
                 bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
+                if constexpr (T::kParam > 0)
+                  bulk_g2s(dst + 2 * T::kSlab, p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g,
+                           T::kParam, &full_bar[s], pol_stream);
               }
             } else {
               if (!*abort_flag) record_error(p.err, PKV_ERR_OOB);
@@ -875,6 +883,24 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty_bar[qs]);
+      // INT8 cache: x = min + q (max - min) / 255 per (block, head), so a score
+      // is dk (q . codes) + k_min sum(q) and p . V is dv (p . codes) + v_min sum(p):
+      // the codes are used as integers and the affine terms added per block
+      constexpr bool kInt8 = T::kParam > 0;
+      float qsum[G], b_run[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        b_run[h] = 0.f;
+        qsum[h] = 0.f;
+        if constexpr (kInt8) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a += qf[h][e];
+#pragma unroll
+          for (int msk = 1; msk < LPT; msk <<= 1) a += __shfl_xor_sync(0xffffffffu, a, msk);
+          qsum[h] = a;
+        }
+      }
 
       float m_run[G], l_part[NF], acc[G][8];
 #pragma unroll
@@ -925,6 +951,22 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
           }
         }
         reduce_scatter<T::kNV, LPT / 2>(part, lane);
+        float4 prm = make_float4(0.f, 0.f, 0.f, 0.f);
+        float dv = 0.f;
+        if constexpr (kInt8) {
+          if (n_valid > 0) prm = *reinterpret_cast<const float4*>(kslab + 2 * T::kSlab);
+          const float dk = (prm.y - prm.x) * (1.f / 255.f);
+          dv = (prm.w - prm.z) * (1.f / 255.f);
+#pragma unroll
+          for (int x = 0; x < NF; ++x) {
+            const int h = (G == 1) ? 0 : (hsel ? NF + x : x);
+            float qs = qsum[0];
+#pragma unroll
+            for (int hh = 1; hh < G; ++hh)
+              if (hh == h) qs = qsum[hh];
+            part[x] = fmaf(part[x], dk, prm.x * qs);
+          }
+        }
 
         // ---- online softmax over the block --------------------------------
         float scv[NF], bm[NF];
@@ -973,9 +1015,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         __syncwarp();
         if (rescale) {
 #pragma unroll
-          for (int h = 0; h < G; ++h)
+          for (int h = 0; h < G; ++h) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[h][e] *= alpha[h];
+            b_run[h] *= alpha[h];
+          }
         }
         // ---- p . V --------------------------------------------------------
 #pragma unroll
@@ -986,6 +1030,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
           float pv[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) pv[h] = pw[t * G + h];
+          if constexpr (kInt8) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              b_run[h] = fmaf(pv[h], prm.z, b_run[h]);
+              pv[h] *= dv;
+            }
+          }
 #pragma unroll
           for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -1000,9 +1051,17 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 #pragma unroll
       for (int msk = LPT; msk < 32; msk <<= 1)
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], msk);
+          if constexpr (kInt8) b_run[h] += __shfl_xor_sync(0xffffffffu, b_run[h], msk);
+        }
+      if constexpr (kInt8) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] += b_run[h];
+      }
 #pragma unroll
       for (int msk = 2; msk < 32; msk <<= 1)
 #pragma unroll

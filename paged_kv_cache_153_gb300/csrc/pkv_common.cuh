@@ -194,6 +194,11 @@ struct E4M3 {
   using storage = uint8_t;
   static constexpr int kBytes = 1;
 };
+// INT8 codes with per-(block, head) min-max scaling: x = min + q (max - min) / 255
+struct U8 {
+  using storage = uint8_t;
+  static constexpr int kBytes = 1;
+};
 
 // two packed 16-bit values -> two floats
 __device__ __forceinline__ float2 unpack2(uint32_t w, F16) {
@@ -228,6 +233,17 @@ __device__ __forceinline__ void load8(const void* p, float* f, E4M3) {
   float2 c = unpack2_e4m3(static_cast<uint16_t>(v.y & 0xffffu));
   float2 d = unpack2_e4m3(static_cast<uint16_t>(v.y >> 16));
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+// eight INT8 codes -> their integer values as floats (exact: 2^23 + q has q
+// in the low mantissa bits)
+__device__ __forceinline__ void load8(const void* p, float* f, U8) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w = i < 4 ? v.x : v.y;
+    f[i] = __uint_as_float(0x4B000000u | ((w >> (8 * (i & 3))) & 0xffu)) - 8388608.0f;
+  }
 }
 
 // two floats -> two E4M3 codes (lo in the low byte), round to nearest even,
