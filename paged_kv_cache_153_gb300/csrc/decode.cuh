@@ -170,9 +170,10 @@ template <int D, int G, int NW, typename KV, bool MMA>
 struct DecodeTraits {
   static constexpr int kEsz = KV::kBytes;
   static constexpr int kSlab = kBlockSize * D * kEsz;          // bytes of one (block, head) slab
-  // INT8 caches stage each block's 16-byte (k_min, k_max, v_min, v_max) after V
+  static constexpr int kStage = 2 * kSlab;                     // K + V
+  // INT8 caches also stage each block's 16-byte (k_min, k_max, v_min, v_max),
+  // into a per-stage slot of its own (the K/V tiles stay 1024-byte aligned)
   static constexpr int kParam = std::is_same<KV, U8>::value ? 16 : 0;
-  static constexpr int kStage = 2 * kSlab + (kParam ? 128 : 0);  // K + V (+ params, padded)
   static constexpr int kTx = 2 * kSlab + kParam;                 // bytes a stage receives
   static constexpr int kSubTiles = (D * kEsz) / 128;           // swizzled [16 x 128 B] tiles per slab
   static constexpr int kQBytes = G * D * 2;
@@ -186,11 +187,11 @@ struct DecodeTraits {
   static_assert(kNF == (G >= 2 ? G / 2 : 1), "lane/head mapping");
   static_assert(!MMA || (G >= 2 && G <= 8 && (D * kEsz) % 128 == 0 && (kEsz == 2 || D * kEsz == 128)),
                 "tensor-core variant");
-  static_assert(!(MMA && kParam), "INT8 caches use the CUDA-core consumer");
 
   // shared memory layout (byte offsets from a 1024-byte aligned base)
   static __host__ __device__ size_t q_off(int stages) { return static_cast<size_t>(stages) * kStage; }
-  static __host__ __device__ size_t p_off(int stages) { return q_off(stages) + 2 * kQBytes; }
+  static __host__ __device__ size_t prm_off(int stages) { return q_off(stages) + 2 * kQBytes; }
+  static __host__ __device__ size_t p_off(int stages) { return prm_off(stages) + static_cast<size_t>(stages) * kParam; }
   static __host__ __device__ size_t merge_off(int stages) {
     return p_off(stages) + sizeof(float) * NW * kBlockSize * G;
   }
@@ -273,6 +274,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(w & 0xffffu)));
   return r;
+}
+// two one-byte codes (bits 0-15 of w) -> packed f16x2, exactly: E4M3 values,
+// or INT8 codes as integers (0x64cc is 1024 + cc in f16; subtracting 1024 is exact)
+__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, E4M3) { return e4m3x2_to_f16x2(w); }
+__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, U8) {
+  const uint32_t r = __byte_perm(w, 0x64u, 0x4140u);
+  uint32_t out;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(r), "r"(0x64006400u));
+  return out;
 }
 
 
@@ -611,6 +621,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
             if (ok) {
               mbar_arrive_expect_tx(&full_bar[s], T::kTx);
+              if constexpr (T::kParam > 0)
+                bulk_g2s(smem + T::prm_off(S) + s * T::kParam,
+                         p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g, T::kParam, &full_bar[s],
+                         pol_stream);
               if constexpr (MMA) {
                 const int y = (ids * p.block_heads + g) * kBlockSize;
 #pragma unroll
@@ -623,9 +637,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                 const int64_t slab = (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab;
                 bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
                 bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
-                if constexpr (T::kParam > 0)
-                  bulk_g2s(dst + 2 * T::kSlab, p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g,
-                           T::kParam, &full_bar[s], pol_stream);
+
               }
             } else {
               if (!*abort_flag) record_error(p.err, PKV_ERR_OOB);
@@ -725,6 +737,22 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty_bar[qs]);
+      // INT8 cache: the MMAs see the codes as integers; a score is
+      // dk (q . codes) + k_min sum(q) and p . V is dv (p . codes) + v_min sum(p)
+      constexpr bool kInt8 = T::kParam > 0;
+      float qs0 = 0.f, qs1 = 0.f, b0r = 0.f, b1r = 0.f;   // sum(q) of heads h0, h0 + 1; v_min sum(p)
+      if constexpr (kInt8) {
+        float a = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const float2 u = unpack2(bq[ks][0], F16{}), v = unpack2(bq[ks][1], F16{});
+          a += (u.x + u.y) + (v.x + v.y);
+        }
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);        // sum(q) of head r4
+        qs0 = __shfl_sync(0xffffffffu, a, 4 * h0);
+        qs1 = __shfl_sync(0xffffffffu, a, 4 * (h0 + 1) < 32 ? 4 * (h0 + 1) : 0);
+      }
       float o[KS][4];
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -759,8 +787,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             ldsm_x4(swz_addr(kslab, krow, 2 * cp + kchunk), r);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t a[4] = {e4m3x2_to_f16x2(r[2 * h2]), e4m3x2_to_f16x2(r[2 * h2 + 1]),
-                                     e4m3x2_to_f16x2(r[2 * h2] >> 16), e4m3x2_to_f16x2(r[2 * h2 + 1] >> 16)};
+              const uint32_t a[4] = {byte2_to_f16x2(r[2 * h2], KV{}), byte2_to_f16x2(r[2 * h2 + 1], KV{}),
+                                     byte2_to_f16x2(r[2 * h2] >> 16, KV{}),
+                                     byte2_to_f16x2(r[2 * h2 + 1] >> 16, KV{})};
               mma16816(c, a, bq[2 * cp + h2][0], bq[2 * cp + h2][1], F16{});
             }
           }
@@ -771,6 +800,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             ldsm_x4(swz_addr(kslab, krow, 2 * ks + kchunk), a);
             mma16816(c, a, bq[ks][0], bq[ks][1], MT{});
           }
+        }
+        float dv = 0.f, vmin = 0.f;
+        if constexpr (kInt8) {
+          const float4 prm = n_valid > 0 ? *reinterpret_cast<const float4*>(smem + T::prm_off(S) + s * T::kParam)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float dk = (prm.y - prm.x) * (1.f / 255.f);
+          dv = (prm.w - prm.z) * (1.f / 255.f);
+          vmin = prm.z;
+          c[0] = fmaf(c[0], dk, prm.x * qs0);
+          c[1] = fmaf(c[1], dk, prm.x * qs1);
+          c[2] = fmaf(c[2], dk, prm.x * qs0);
+          c[3] = fmaf(c[3], dk, prm.x * qs1);
         }
         const bool v0 = r4 < n_valid, v1 = r4 + 8 < n_valid;
         const float s00 = v0 ? c[0] * sc : -INFINITY, s01 = v0 ? c[1] * sc : -INFINITY;
@@ -791,9 +832,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         constexpr bool kSplitP = std::is_same<MT, BF16>::value;
         const float e00 = exp2f(s00 - ref0), e01 = exp2f(s01 - ref1);
         const float e10 = exp2f(s10 - ref0), e11 = exp2f(s11 - ref1);
-        const uint32_t x0 = pack2(e00, e01, MT{});   // tokens 0..7
-        const uint32_t x1 = pack2(e10, e11, MT{});   // tokens 8..15
-        const float2 p0 = unpack2(x0, MT{}), p1 = unpack2(x1, MT{});
+        // (INT8: the MMA multiplies the codes by p dv; the v_min sum(p) part is kept apart)
+        const float ps = kInt8 ? dv : 1.f;
+        const uint32_t x0 = pack2(e00 * ps, e01 * ps, MT{});   // tokens 0..7
+        const uint32_t x1 = pack2(e10 * ps, e11 * ps, MT{});   // tokens 8..15
+        const float2 p0 = kInt8 ? make_float2(e00, e01) : unpack2(x0, MT{});
+        const float2 p1 = kInt8 ? make_float2(e10, e11) : unpack2(x1, MT{});
         uint32_t x0l = 0u, x1l = 0u;
         float2 r0 = make_float2(0.f, 0.f), r1 = make_float2(0.f, 0.f);
         if constexpr (kSplitP) {
@@ -805,6 +849,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         // l sums exactly what is multiplied
         l0 = l0 * a0 + ((p0.x + r0.x) + (p1.x + r1.x));
         l1 = l1 * a1 + ((p0.y + r0.y) + (p1.y + r1.y));
+        if constexpr (kInt8) {
+          b0r = b0r * a0 + (p0.x + p1.x) * vmin;
+          b1r = b1r * a1 + (p0.y + p1.y) * vmin;
+        }
         const bool resc = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
         m0 = mn0;
         m1 = mn1;
@@ -829,10 +877,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             ldsm_x4(swz_addr(vslab, krow, 2 * cp + kchunk), r);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t a[4] = {movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2])),
-                                     movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2] >> 16)),
-                                     movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2 + 1])),
-                                     movmatrix_trans(e4m3x2_to_f16x2(r[2 * h2 + 1] >> 16))};
+              const uint32_t a[4] = {movmatrix_trans(byte2_to_f16x2(r[2 * h2], KV{})),
+                                     movmatrix_trans(byte2_to_f16x2(r[2 * h2] >> 16, KV{})),
+                                     movmatrix_trans(byte2_to_f16x2(r[2 * h2 + 1], KV{})),
+                                     movmatrix_trans(byte2_to_f16x2(r[2 * h2 + 1] >> 16, KV{}))};
               mma16816(o[2 * cp + h2], a, b0, b1, F16{});
             }
           }
@@ -854,6 +902,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       for (int msk = 4; msk < 32; msk <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
         l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
+        if constexpr (kInt8) {
+          b0r += __shfl_xor_sync(0xffffffffu, b0r, msk);
+          b1r += __shfl_xor_sync(0xffffffffu, b1r, msk);
+        }
+      }
+      if constexpr (kInt8) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][0] += b0r; o[mt][1] += b1r; o[mt][2] += b0r; o[mt][3] += b1r;
+        }
       }
       if (h0 < G) {
 #pragma unroll
@@ -954,7 +1012,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         float4 prm = make_float4(0.f, 0.f, 0.f, 0.f);
         float dv = 0.f;
         if constexpr (kInt8) {
-          if (n_valid > 0) prm = *reinterpret_cast<const float4*>(kslab + 2 * T::kSlab);
+          if (n_valid > 0) prm = *reinterpret_cast<const float4*>(smem + T::prm_off(S) + s * T::kParam);
           const float dk = (prm.y - prm.x) * (1.f / 255.f);
           dv = (prm.w - prm.z) * (1.f / 255.f);
 #pragma unroll
