@@ -62,15 +62,31 @@ def describe(w: wl.Workload) -> dict:
     }
 
 
-def kernel_source_digest() -> str:
+# the sources each timed kernel is built from: a committed DRAM-traffic figure
+# stays valid while these files are unchanged
+_COMMON_SOURCES = ("pkv_common.cuh", "host_util.h")
+_DECODE_SOURCES = ("api.cu", "decode.cuh", "decode_launch.cuh", "decode_f16.cu", "decode_bf16.cu",
+                   "decode_e4m3.cu", "decode_int8.cu")
+KERNEL_SOURCES = {
+    "decode": _COMMON_SOURCES + _DECODE_SOURCES,
+    "int8": _COMMON_SOURCES + _DECODE_SOURCES + ("append.cu", "append_int8.cu"),
+    "cow": _COMMON_SOURCES + ("append.cu",),
+    "prefill": _COMMON_SOURCES + ("prefill.cu",),
+}
+
+
+def kernel_source_digest(family: str = "decode") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_153_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in sorted(KERNEL_SOURCES[family]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def source_family(workload: str) -> str:
+    return workload if workload in KERNEL_SOURCES else "decode"
 
 
 def measured_peak():
@@ -83,15 +99,15 @@ def measured_peak():
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from a committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+    """DRAM bytes per timed call from a committed ncu summary, if it was taken
+    on the current source of the kernels the workload runs (else None)."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
     entry = rec.get(workload)
-    if not entry or entry.get("source_digest") != kernel_source_digest():
+    if not entry or entry.get("source_digest") != kernel_source_digest(source_family(workload)):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -600,7 +616,7 @@ def run_int8(args, rank: int, local_rank: int) -> dict | None:
                        "head) min-max scalars (bf16 q/out)", step="slot mapping + INT8 append (re-quantising the "
                        "block) + INT8 paged decode attention (decode + combine)"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "the step's four launches, average over the timed region",
+                     "traffic": ncu_traffic("int8"), "kernel": "the step's four launches, average over the timed region",
                      "algorithmic_bytes_per_launch": algo, "avg_launch_ms": per_ms,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth"},
         "gpu_launches": 4 * args.steps, "clocks": clocks.summary(), "e2e": None,
