@@ -15,30 +15,37 @@
 // r / G, head r % G), so one K/V tile serves the whole GQA group.  Key tiles
 // are 128 keys = 8 cache blocks, gathered through the block table by tiled TMA
 // loads of [16 rows x 128 B] boxes into the 128-byte swizzled K-major layout
-// the tensor cores read.  Per key tile:
-//   S = Q K^T     tcgen05.mma kind::f16, M = N = 128, 8 k-steps of 16, fp32 in TMEM
+// the tensor cores read.  Per key tile j:
+//   S = Q K^T     tcgen05.mma kind::f16, M = N = 128, 8 k-steps of 16, fp32
+//                 into TMEM buffer j % 3
 //   softmax       8 warps, two threads per row (warps w and w + 4 share TMEM
-//                 lane quarter w % 4; each takes 64 of the 128 columns and both
-//                 take the row maximum over all of them): tcgen05.ld of S, mask,
-//                 online max / sum in the log2 domain, P stored to shared
-//                 memory in the input type (K-major, swizzled); when a row's
-//                 max grows its O row in TMEM is rescaled (ld, scale, st)
-//   O += P V      tcgen05.mma with V as an MN-major operand (keys x head_dim as
-//                 staged), fp32 in TMEM.  bf16 keeps only 8 significant bits,
-//                 so for bf16 P is split into P_hi = bf16(p) and
+//                 lane quarter w % 4, each owns 64 of the 128 columns): one
+//                 tcgen05.ld of its columns, mask, partial row maximum, which
+//                 the two threads of a row exchange through shared memory;
+//                 P = 2^(s scale log2 e - m) is written back into the same
+//                 TMEM columns in the input type (tcgen05.st)
+//   O += P V      tcgen05.mma with A = P read from TMEM and B = V as an
+//                 MN-major shared-memory operand (keys x head_dim as staged),
+//                 fp32 in TMEM.  bf16 keeps only 8 significant bits, so for
+//                 bf16 P is split into P_hi (p truncated to bf16) and
 //                 P_lo = bf16(p - P_hi) and both are multiplied (two MMA
-//                 passes): P is then exact to ~2^-17 relative, where a single
+//                 passes): P is then exact to ~2^-16 relative, where a single
 //                 bf16 rounding (2^-9) could exceed the 2e-3 tolerance on
 //                 outputs of a few keys.  fp16 P (2^-12) needs one pass.
-// Warp roles: warps 0-7 softmax and epilogue, warp 8 TMA producer (a 2-stage
-// ring with separate K and V barriers: K of tile j + 2 is loaded as soon as
-// Q K^T of tile j is done, V once P V of tile j is), warp 9 TMEM owner and
-// MMA issuer (one elected lane).  S has two
-// TMEM buffers: the MMA warp issues Q K^T of tile j+1 before it waits for the
-// softmax of tile j, so the tensor cores compute the next scores while the
-// softmax warps work.  Every wait
-// is bounded; on expiry the block records PKV_ERR_TIMEOUT, drains what it has
-// in flight and frees its TMEM.
+//                 The softmax arithmetic runs on packed fp32 pairs.
+// P overwrites its own S in TMEM: the 32 columns of each 32-key chunk hold its
+// P_hi pairs in the first 16 and its P_lo pairs in the next 16, so a thread
+// only ever writes columns it has already read.  With three S / P buffers the
+// scores of tile j + 2 are computed while the softmax of tile j + 1 and the
+// P V of tile j run.  The row reference m moves only when a tile's maximum
+// exceeds it by more than 2^8 (P stays <= 256, exact in fp32 accumulation):
+// only then is the O row rescaled, after the previous P V has completed, so
+// in the steady state the softmax never waits for the tensor cores.
+// Warp roles: warps 0-7 softmax and epilogue, warp 8 TMA producer (K in a
+// 3-stage ring, V in a 2-stage ring, issued in the order the MMAs consume
+// them: V of tile j, then K of tile j + 2), warp 9 TMEM owner and MMA issuer
+// (one elected lane).  Every wait is bounded; on expiry the block records
+// PKV_ERR_TIMEOUT, drains what it has in flight and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -70,16 +77,22 @@ struct PrefillParams {
 constexpr int kPM = 128;                  // query rows per tile
 constexpr int kPN = 128;                  // keys per tile
 constexpr int kPD = 128;                  // head_dim
-constexpr int kTile = kPM * kPD * 2;      // bytes of a 128 x 128 16-bit tile (Q, P, K or V)
+constexpr int kTile = kPM * kPD * 2;      // bytes of a 128 x 128 16-bit tile (Q, K or V)
 constexpr int kPThreads = 320;           // 8 softmax warps, 1 TMA warp, 1 MMA warp
 constexpr int kSoftmax = 256;            // softmax threads: 2 per query row
-constexpr int kTmemCols = 512;            // S of even tiles: 0-127, O: 128-255, S of odd tiles: 256-383
-constexpr size_t kPrefillSmem = 7 * static_cast<size_t>(kTile) + 256 + 1024;
+constexpr int kSBufs = 3;                 // S / P buffers in TMEM
+constexpr int kKStages = 3, kVStages = 2; // K and V rings in shared memory
+constexpr int kTmemCols = 512;            // S / P buffers at columns 0, 128, 256; O at 384
+constexpr int kOCol = kSBufs * kPN;
+constexpr float kRescaleLog2 = 8.f;      // the row reference moves when the max outgrows it by > 2^8
 
-// offsets in the 1024-aligned shared block: Q | P (hi part) | P (lo part) | K0 V0 | K1 V1 | barriers
-constexpr int kOffQ = 0, kOffP = kTile, kOffPlo = 2 * kTile;
-constexpr int kOffKV = 3 * kTile;   // stage s: K at kOffKV + 2 s kTile, V after it
-constexpr int kOffBar = 7 * kTile;
+// offsets in the 1024-aligned shared block: Q | K x 3 | V x 2 | barriers | row exchange
+constexpr int kOffQ = 0;
+constexpr int kOffK = kTile;                          // stage s at kOffK + s kTile
+constexpr int kOffV = kOffK + kKStages * kTile;       // stage s at kOffV + s kTile
+constexpr int kOffBar = kOffV + kVStages * kTile;
+constexpr int kOffRed = kOffBar + 256;                // float [3][2][128]: row maxima (2 slots), row sums
+constexpr size_t kPrefillSmem = static_cast<size_t>(kOffRed) + 3 * 2 * kPM * 4 + 1024;
 
 // ---------------------------------------------------------------------------
 // tcgen05 helpers
@@ -105,6 +118,17 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+
+// the same with A read from TMEM (lane m = row m, column c holding the 16-bit
+// pair of k = 2c, 2c + 1 of the 16-wide k-step, low half first)
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
       : "memory");
 }
 
@@ -159,6 +183,111 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 / 32 consecutive 32-bit columns of this thread's TMEM lane (no wait)
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait.
+// The wait names the loaded registers as operands so that no use of them is
+// scheduled before it.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]), "=r"(r[32 * h + 4]),
+          "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]), "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]),
+          "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]), "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]),
+          "=r"(r[32 * h + 14]), "=r"(r[32 * h + 15]), "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]),
+          "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]), "=r"(r[32 * h + 20]), "=r"(r[32 * h + 21]),
+          "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]), "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]),
+          "=r"(r[32 * h + 26]), "=r"(r[32 * h + 27]), "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]),
+          "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(taddr + 32 * h));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+  asm volatile(""
+               : "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]),
+                 "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]),
+                 "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]),
+                 "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]),
+                 "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// packed fp32 pairs (the f32x2 instructions of this architecture)
+__device__ __forceinline__ uint64_t f32x2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f32x2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// maximum of 64 values: eight independent chains, then a short tree
+__device__ __forceinline__ float max64(const float* v) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float* x = v + 8 * k;
+    m[k] = fmaxf(fmax3(fmax3(x[0], x[1], x[2]), x[3], x[4]), fmax3(x[5], x[6], x[7]));
+  }
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
 // byte offset of 16-byte chunk c (elements 8c..8c+7) of row r in a 128 x 128
 // 16-bit tile stored K-major with the 128-byte swizzle: two 64-column halves of
 // 16 KiB, 8-row atoms of 1 KiB, chunk index XOR row within the atom
@@ -172,20 +301,22 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 template <typename QT, int G>
 __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __grid_constant__ PrefillParams p) {
   constexpr int TPT = kPM / G;                       // tokens per query tile
+  constexpr bool kSplit = std::is_same<QT, BF16>::value;
   extern __shared__ unsigned char psm_raw[];
   unsigned char* sm = psm_raw + ((1024 - (smem_u32(psm_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint64_t* k_full = bars;           // [2] per stage: K of the stage's tile landed
-  uint64_t* v_full = bars + 2;       // [2] V landed
-  uint64_t* k_empty = bars + 4;      // [2] Q K^T of the stage's tile done: K may be reloaded
-  uint64_t* v_empty = bars + 6;      // [2] P V done: V may be reloaded
-  uint64_t* s_full = bars + 8;       // [2], one per S buffer
-  uint64_t* p_full = bars + 10;      // kSoftmax arrivals
-  uint64_t* pv_done = bars + 11;
-  uint64_t* q_ready = bars + 12;     // kSoftmax arrivals
-  uint64_t* mma_idle = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 15);
+  uint64_t* k_full = bars;                 // [3] K of the stage's tile landed
+  uint64_t* k_empty = bars + 3;            // [3] Q K^T of the stage's tile done: K may be reloaded
+  uint64_t* v_full = bars + 6;             // [2] V landed
+  uint64_t* v_empty = bars + 8;            // [2] P V done: V may be reloaded
+  uint64_t* s_full = bars + 10;            // [3] per S / P buffer: scores ready
+  uint64_t* p_full = bars + 13;            // [3] per buffer, kSoftmax arrivals: P written, O rescaled
+  uint64_t* pv_done = bars + 16;           // [3] per buffer: P V of its tile done
+  uint64_t* q_ready = bars + 19;           // kSoftmax arrivals
+  uint64_t* mma_idle = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
+  float* red = reinterpret_cast<float*>(sm + kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
@@ -215,16 +346,19 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   }
   if (tid == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, kSoftmax);
-    mbar_init(pv_done, 1);
+    for (int s = 0; s < kSBufs; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], kSoftmax);
+      mbar_init(&pv_done[s], 1);
+    }
     mbar_init(q_ready, kSoftmax);
     mbar_init(mma_idle, 1);
     fence_mbar_init();
@@ -233,13 +367,14 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_o = tmem + kPN;
-  auto t_s = [&](int j) -> uint32_t { return tmem + ((j & 1) ? 2 * kPN : 0); };
+  const uint32_t t_o = tmem + kOCol;
+  auto t_s = [&](int j) -> uint32_t { return tmem + (j % kSBufs) * kPN; };
 
   if (warp < 8) {
     // ============================ softmax / epilogue ============================
     const int r = tid & (kPM - 1);                     // row = TMEM lane
-    const int half = tid >> 7;                         // columns [64 half, 64 half + 64) of S, P and O
+    const int half = tid >> 7;                         // columns [64 half, 64 half + 64) of S and O
+    const int pair_bar = 2 + (warp & 3);               // named barrier of warps w and w + 4 (one row each)
     const int tok = i0 + r / G, head = g * G + r % G;
     const bool row_live = tok < i1;
     const int pos = row_live ? q_start + tok : -1;
@@ -259,97 +394,109 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
       mbar_arrive(q_ready);
     }
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float m_run = -INFINITY, l_run = 0.f;
+    const int col0 = 64 * half;
+    float m_ref = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      // waits are made warp-uniform: the tcgen05.ld / st below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err))) { ok = false; break; }
-      tc_fence_after();
-      // Two passes over the S row in chunks of 32 columns, re-read from TMEM
-      // (a compact loop: the fully unrolled row did not fit the instruction
-      // cache).  Only tiles that reach past a row's position need the mask.
-      const bool masked = __any_sync(0xffffffffu, j * kPN + kPN - 1 > pos);   // (for pass 1; pass 2 re-tests)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kPN; c0 += 32) {
-        float v[32];
-        tmem_ld32(t_s(j) + lane_base + c0, v);
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = (j * kPN + c0 + i <= pos) ? v[i] : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
-      }
-      // scores in the log2 domain: s * scale * log2(e) (the scale is positive,
-      // so the maximum commutes with it)
-      const float m_new = fmaxf(m_run, mx * p.qk_scale_log2);
-      const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - ref);
-      // O and the P buffer are free once the previous p.V has completed
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, p.err))) { ok = false; break; }
+    // A failed wait is published at the next row exchange, where both warps of
+    // the pair see it and leave together (a warp must never leave its partner
+    // waiting at the named barrier).
+    for (int j = 0; j < n_tiles; ++j) {
+      const int buf = j % kSBufs, ph = (j / kSBufs) & 1;
+      const uint32_t ts = t_s(j) + lane_base + col0;
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[buf], ph, p.err));
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
-            float o[32];
-            tmem_ld32(t_o + lane_base + c0, o);
+      }
+      float v[64];
+      float mx = -INFINITY;
+      if (ok) {
+        tmem_ld64(ts, v);
+        // only tiles reaching past a row's position need the causal mask
+        if (__any_sync(0xffffffffu, j * kPN + kPN - 1 > pos)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(t_o + lane_base + c0, o);
-          }
+          for (int i = 0; i < 64; ++i) v[i] = (j * kPN + col0 + i <= pos) ? v[i] : -INFINITY;
+        }
+        mx = max64(v);
+        red[((j & 1) * 2 + half) * kPM + r] = mx;
+      }
+      if (named_bar_red_or(pair_bar, 64, !ok)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, red[((j & 1) * 2 + (1 - half)) * kPM + r]);
+      // scores in the log2 domain: s * scale * log2(e) (the scale is positive,
+      // so the maximum commutes with it).  The reference moves only when the
+      // tile's maximum outgrows it by more than 2^8 (always on a row's first
+      // unmasked tile, where m_ref = -inf and alpha = 0).
+      const float m_tile = mx * p.qk_scale_log2;
+      float alpha = 1.f;
+      if (m_tile > m_ref + kRescaleLog2) {
+        alpha = ex2_approx(m_ref - m_tile);
+        m_ref = m_tile;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O may be touched once the previous tile's P V has completed
+        const int pb = (j - 1) % kSBufs;
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[pb], ((j - 1) / kSBufs) & 1, p.err))) {
+          ok = false;
+          continue;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = col0; c0 < col0 + 64; c0 += 32) {
+          float o[32];
+          tmem_ld32(t_o + lane_base + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(t_o + lane_base + c0, o);
         }
       }
-      constexpr bool kSplit = std::is_same<QT, BF16>::value;
-      float psum = 0.f;
-      const float nref = -ref;
-#pragma unroll 1
-      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
-        float v[32];
-        tmem_ld32(t_s(j) + lane_base + c0, v);
-        uint32_t hi[16], lo[16];
+      // P over this thread's two 32-key chunks, written over the chunk's own
+      // columns: 16 pairs of P_hi, then (bf16) 16 pairs of P_lo.  Masked scores
+      // are -inf and give 2^-inf = 0.  For bf16, P_hi is p truncated to bf16
+      // (its top 16 bits) and P_lo = bf16(p - P_hi), where p - P_hi is exact.
+      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const uint64_t scale2 = f32x2(p.qk_scale_log2, p.qk_scale_log2), nref2 = f32x2(nref, nref);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // (+0, +0) pairs
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float e0 = ex2_approx(fmaf(v[i], p.qk_scale_log2, nref));
-          float e1 = ex2_approx(fmaf(v[i + 1], p.qk_scale_log2, nref));
-          if (masked) {
-            e0 = (j * kPN + c0 + i <= pos) ? e0 : 0.f;
-            e1 = (j * kPN + c0 + i + 1 <= pos) ? e1 : 0.f;
-          }
-          psum += e0 + e1;
-          hi[i / 2] = pack2(e0, e1, QT{});
+          const float2 x = f32x2_split(fma_f32x2(f32x2(v[32 * c + i], v[32 * c + i + 1]), scale2, nref2));
+          const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
+          const uint64_t e01 = f32x2(e0, e1);
+          acc[(i / 2) & 3] = add_f32x2(acc[(i / 2) & 3], e01);
           if constexpr (kSplit) {
-            const float2 b = unpack2(hi[i / 2], QT{});
-            lo[i / 2] = pack2(e0 - b.x, e1 - b.y, QT{});
+            const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
+            pk[i / 2] = __byte_perm(b0, b1, 0x7632);
+            const float2 lo = f32x2_split(
+                sub_f32x2(e01, f32x2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u))));
+            pk[16 + i / 2] = pack2(lo.x, lo.y, QT{});
+          } else {
+            pk[i / 2] = pack2(e0, e1, QT{});
           }
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t off = tile_off(r, c0 / 8 + c);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffP) + off),
-                       "r"(hi[4 * c]), "r"(hi[4 * c + 1]), "r"(hi[4 * c + 2]), "r"(hi[4 * c + 3])
-                       : "memory");
-          if constexpr (kSplit)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(sm + kOffPlo) + off),
-                         "r"(lo[4 * c]), "r"(lo[4 * c + 1]), "r"(lo[4 * c + 2]), "r"(lo[4 * c + 3])
-                         : "memory");
-        }
+        if constexpr (kSplit)
+          tmem_st32u(ts + 32 * c, pk);
+        else
+          tmem_st16u(ts + 32 * c, pk);
       }
+      const float2 s0 = f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])));
+      const float psum = s0.x + s0.y;
+      tmem_wait_st();
       // l sums the fp32 weights (the multiplied hi + lo, or fp16, parts match
-      // them to ~2^-17 / 2^-12 relative)
+      // them to ~2^-16 / 2^-12 relative)
       l_run = l_run * alpha + psum;
-      m_run = m_new;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[buf]);
     }
     if (!ok) *abort_flag = 1;
-    // epilogue: out = O / l.  The two threads of a row hold the sums of their
-    // halves; they meet in the P buffer, free once the last p.V is done.
+    // epilogue: out = O / l.  The two threads of a row add their halves' sums.
     ok = __all_sync(0xffffffffu, ok);
-    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1, p.err));
-    float* lx = reinterpret_cast<float*>(sm + kOffP);
+    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(&pv_done[(n_tiles - 1) % kSBufs],
+                                                             ((n_tiles - 1) / kSBufs) & 1, p.err));
+    float* lx = red + 4 * kPM;
     lx[half * kPM + r] = l_run;
     named_bar_sync(1, kSoftmax);
     const float l_tot = l_run + lx[(1 - half) * kPM + r];
@@ -359,7 +506,7 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
       auto* dst = reinterpret_cast<uint4*>(static_cast<typename QT::storage*>(p.out) +
                                            ((static_cast<int64_t>(cu0) + tok) * p.n_q_heads + head) * kPD);
 #pragma unroll 1
-      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+      for (int c0 = col0; c0 < col0 + 64; c0 += 32) {
         float o[32];
         tmem_ld32(t_o + lane_base + c0, o);
         if (row_live) {
@@ -378,9 +525,9 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     // ============================ TMA producer ============================
     const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by the other query tiles
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    int j = 0, issued_k = 0, issued_v = 0;
-    for (; j < n_tiles && !*abort_flag; ++j) {
-      const int s = j & 1;
+    // cache row of this lane's block of key tile j (a block past the context,
+    // or a bad id, is read from rows outside the tensor, which TMA fills with zeros)
+    auto tile_row = [&](int j) -> int {
       int id = -1;
       if (lane < kPN / kBlockSize) {
         const int blk = j * (kPN / kBlockSize) + lane;
@@ -390,83 +537,88 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
           id = -1;
         }
       }
-      // a block past the context (or a bad id) is read from rows outside the
-      // tensor, which TMA fills with zeros
-      const int y = (id >= 0) ? (id * p.n_kv_heads + g) * kBlockSize : -2 * kBlockSize;
-      unsigned char* kd = sm + kOffKV + 2 * s * kTile + lane * 2048;
-      unsigned char* vd = kd + kTile;
-      // K, then V, each after its previous use in this stage is done
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, p.err))) {
-        *abort_flag = 1;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[s], kTile);
+      return (id >= 0) ? (id * p.n_kv_heads + g) * kBlockSize : -2 * kBlockSize;
+    };
+    // load K (is_v = 0) or V of key tile j into its ring stage, after the
+    // stage's previous tile has been consumed
+    int issued_k = 0, issued_v = 0;
+    auto load = [&](int j, bool is_v) -> bool {
+      const int stages = is_v ? kVStages : kKStages;
+      const int s = j % stages;
+      uint64_t* full = is_v ? &v_full[s] : &k_full[s];
+      uint64_t* empty = is_v ? &v_empty[s] : &k_empty[s];
+      if (j >= stages && !__all_sync(0xffffffffu, mbar_wait(empty, ((j / stages) - 1) & 1, p.err))) return false;
+      const int y = tile_row(j);
+      if (lane == 0) mbar_arrive_expect_tx(full, kTile);
       __syncwarp();
       if (lane < kPN / kBlockSize) {
+        unsigned char* dst = sm + (is_v ? kOffV : kOffK) + s * kTile + lane * 2048;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) tma_load_2d(kd + h * (kTile / 2), &p.tmap_k, h * 64, y, &k_full[s], pol);
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d(dst + h * (kTile / 2), is_v ? &p.tmap_v : &p.tmap_k, h * 64, y, full, pol);
       }
       __syncwarp();
-      issued_k = j + 1;
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, p.err))) {
-        *abort_flag = 1;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[s], kTile);
-      __syncwarp();
-      if (lane < kPN / kBlockSize) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) tma_load_2d(vd + h * (kTile / 2), &p.tmap_v, h * 64, y, &v_full[s], pol);
-      }
-      __syncwarp();
-      issued_v = j + 1;
+      (is_v ? issued_v : issued_k) = j + 1;
+      return true;
+    };
+    // the order the MMAs consume them in: K0, K1, then V of tile j and K of tile j + 2
+    bool good = load(0, false) && (n_tiles < 2 || load(1, false));
+    for (int j = 0; good && j < n_tiles && !*abort_flag; ++j) {
+      good = load(j, true) && (j + 2 >= n_tiles || load(j + 2, false));
     }
+    if (!good) *abort_flag = 1;
     if (*abort_flag && lane == 0) {
       // loads this warp issued that nobody consumed: wait for them (bounded)
       const unsigned long long deadline = global_ns() + kWaitLimitNs;
-      for (int jj = max(0, issued_k - 2); jj < issued_k; ++jj)
-        mbar_wait_until(&k_full[jj & 1], (jj >> 1) & 1, deadline);
-      for (int jj = max(0, issued_v - 2); jj < issued_v; ++jj)
-        mbar_wait_until(&v_full[jj & 1], (jj >> 1) & 1, deadline);
+      for (int jj = max(0, issued_k - kKStages); jj < issued_k; ++jj)
+        mbar_wait_until(&k_full[jj % kKStages], (jj / kKStages) & 1, deadline);
+      for (int jj = max(0, issued_v - kVStages); jj < issued_v; ++jj)
+        mbar_wait_until(&v_full[jj % kVStages], (jj / kVStages) & 1, deadline);
     }
   } else {
-    // ============================ MMA issuer (warp 5) ============================
-    const uint32_t sq = smem_u32(sm + kOffQ), sp = smem_u32(sm + kOffP), splo = smem_u32(sm + kOffPlo);
-    constexpr int kPasses = std::is_same<QT, BF16>::value ? 2 : 1;   // P_hi, then P_lo
+    // ============================ MMA issuer (warp 9) ============================
+    // One elected lane waits, issues and commits.  A tcgen05.commit holds its
+    // thread until the MMA queue ahead of the tensor cores has drained to a few
+    // MMAs, so each batch is committed at once and the next one's waits are
+    // short (their phases have completed by then).
+    const uint32_t sq = smem_u32(sm + kOffQ);
+    constexpr int kPasses = kSplit ? 2 : 1;   // P_hi, then P_lo
     constexpr uint32_t kIdQK = umma_idesc<QT>(false), kIdPV = umma_idesc<QT>(true);
     bool ok = true;
     if (lane == 0) ok = mbar_wait(q_ready, 0, p.err);
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    // S = Q K^T of tile j into S buffer j & 1 (its previous tile's softmax has
-    // finished reading it: the p_full wait of that tile came before)
+    // S = Q K^T of tile j into S buffer j % 3 (its previous tile's P V has
+    // completed: checked by the caller)
     auto issue_qk = [&](int j) -> bool {
-      const int s = j & 1;
+      const int s = j % kKStages;
       bool good = true;
-      if (lane == 0) good = mbar_wait(&k_full[s], (j >> 1) & 1, p.err);
+      if (lane == 0) good = mbar_wait(&k_full[s], (j / kKStages) & 1, p.err);
       good = __shfl_sync(0xffffffffu, good, 0);
       if (good && lane == 0) {
-        const uint32_t sk = smem_u32(sm + kOffKV + 2 * s * kTile);
+        // descriptors built once per tile; each k-step adds a compile-time
+        // offset to the address field (addr >> 4, no carry out of its 14 bits
+        // for shared addresses below 256 KiB)
+        const uint64_t a0 = umma_desc(sq, 16, 1024), b0 = umma_desc(smem_u32(sm + kOffK + s * kTile), 16, 1024);
+        const uint32_t d = t_s(j);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kPD / 16; ++ks) {
-          const uint32_t koff = (ks >> 2) * (kTile / 2) + (ks & 3) * 32;
-          umma_f16(t_s(j), umma_desc(sq + koff, 16, 1024), umma_desc(sk + koff, 16, 1024), kIdQK, ks > 0);
+          const uint64_t koff = static_cast<uint64_t>(((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4);
+          umma_f16(d, a0 + koff, b0 + koff, kIdQK, ks > 0);
         }
-        umma_commit(&s_full[s]);
+        umma_commit(&s_full[j % kSBufs]);
         umma_commit(&k_empty[s]);
       }
       __syncwarp();
       return good;
     };
     if (ok && n_tiles > 0) ok = issue_qk(0);
+    if (ok && n_tiles > 1) ok = issue_qk(1);
     for (int j = 0; j < n_tiles && ok && !*abort_flag; ++j) {
-      const int s = j & 1;
-      const uint32_t sv = smem_u32(sm + kOffKV + 2 * s * kTile) + kTile;
-      if (j + 1 < n_tiles && !issue_qk(j + 1)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) ok = mbar_wait(p_full, j & 1, p.err) && mbar_wait(&v_full[s], (j >> 1) & 1, p.err);
+      const int buf = j % kSBufs, vs = j % kVStages;
+      const uint32_t sv = smem_u32(sm + kOffV + vs * kTile);
+      if (lane == 0)
+        ok = mbar_wait(&p_full[buf], (j / kSBufs) & 1, p.err) && mbar_wait(&v_full[vs], (j / kVStages) & 1, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       // the tile holding the context's last, partial block: its rows past the
@@ -483,18 +635,32 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
       }
       if (lane == 0) {
         tc_fence_after();
+        // k-step ks takes keys 16 ks .. 16 ks + 15: chunk ks / 2, columns
+        // 8 (ks % 2) of its P_hi half (pass 0) or P_lo half (pass 1)
+        const uint64_t b0 = umma_desc(sv, kTile / 2, 1024);
+        const uint32_t a0 = t_s(j);
 #pragma unroll
         for (int pass = 0; pass < kPasses; ++pass)
 #pragma unroll
-          for (int ks = 0; ks < kPN / 16; ++ks) {
-            const uint32_t poff = (ks >> 2) * (kTile / 2) + (ks & 3) * 32;
-            umma_f16(t_o, umma_desc((pass ? splo : sp) + poff, 16, 1024),
-                     umma_desc(sv + ks * 2048, kTile / 2, 1024), kIdPV, j > 0 || ks > 0 || pass > 0);
-          }
-        umma_commit(pv_done);
-        umma_commit(&v_empty[s]);
+          for (int ks = 0; ks < kPN / 16; ++ks)
+            umma_f16_tmem_a(t_o, a0 + 32 * (ks >> 1) + 16 * pass + 8 * (ks & 1),
+                            b0 + static_cast<uint64_t>((ks * 2048) >> 4), kIdPV, j > 0 || ks > 0 || pass > 0);
+        umma_commit(&pv_done[buf]);
+        umma_commit(&v_empty[vs]);
       }
       __syncwarp();
+      // S of tile j + 2 goes to the buffer of tile j - 1, free once its P V is done
+      if (j + 2 < n_tiles) {
+        if (j >= 1) {
+          if (lane == 0) ok = mbar_wait(&pv_done[(j - 1) % kSBufs], ((j - 1) / kSBufs) & 1, p.err);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+        if (!issue_qk(j + 2)) {
+          ok = false;
+          break;
+        }
+      }
     }
     if (!ok) *abort_flag = 1;
     // every MMA this thread issued has completed before TMEM is released
@@ -504,7 +670,6 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     }
     __syncwarp();
   }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
