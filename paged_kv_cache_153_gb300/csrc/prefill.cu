@@ -78,7 +78,7 @@ constexpr int kPM = 128;                  // query rows per tile
 constexpr int kPN = 128;                  // keys per tile
 constexpr int kPD = 128;                  // head_dim
 constexpr int kTile = kPM * kPD * 2;      // bytes of a 128 x 128 16-bit tile (Q, K or V)
-constexpr int kPThreads = 320;           // 8 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kPThreads = 352;           // 8 softmax warps, 1 TMA warp, 2 MMA warps
 constexpr int kSoftmax = 256;            // softmax threads: 2 per query row
 constexpr int kSBufs = 3;                 // S / P buffers in TMEM
 constexpr int kKStages = 3, kVStages = 2; // K and V rings in shared memory
@@ -136,6 +136,39 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// arrive on `bar` in both CTAs of the cluster (same shared offset) once every
+// tcgen05 operation issued so far by this thread has completed
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// tiled TMA load written to the same shared offset of both CTAs of the cluster,
+// completing on the barrier at `bar`'s offset in each
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3)),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+
+// every thread of both CTAs of the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = 0)
@@ -313,9 +346,10 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   uint64_t* p_full = bars + 13;            // [3] per buffer, kSoftmax arrivals: P written, O rescaled
   uint64_t* pv_done = bars + 16;           // [3] per buffer: P V of its tile done
   uint64_t* q_ready = bars + 19;           // kSoftmax arrivals
-  uint64_t* mma_idle = bars + 20;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
+  uint64_t* mma_idle = bars + 20;          // Q K^T issuer drained
+  uint64_t* pv_idle = bars + 21;           // P V issuer drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 23);
   float* red = reinterpret_cast<float*>(sm + kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -326,16 +360,25 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   const int cu0 = p.cu_seqlens[b];
   const int n_new = p.cu_seqlens[b + 1] - cu0;
   const int ctx = p.context_lens[b];
-  const int i0 = qt * TPT;
-  if (i0 >= n_new) return;                            // whole block: no tile here
-  const int i1 = min(n_new, i0 + TPT);
   const int q_start = ctx - n_new;                    // position of new token 0
+  // (the same decision in both CTAs of the cluster: they share the sequence)
   if (q_start < 0 || ctx > p.max_blocks_per_seq * kBlockSize) {
     if (tid == 0) record_error(p.err, PKV_ERR_OOB);
     return;
   }
-  const int last_pos = q_start + i1 - 1;
-  const int n_tiles = last_pos / kPN + 1;
+  // The two CTAs of a cluster hold adjacent query tiles of one (sequence, KV
+  // head): rank 0 the later one.  Each loads half of every K / V tile into
+  // both, so both run the key tiles of the longer one (the shorter one's rows
+  // see the extra keys masked).
+  const int rank = cluster_rank();
+  auto tiles_of = [&](int qtile) -> int {
+    const int a = qtile * TPT;
+    return (qtile < 0 || a >= n_new) ? 0 : (q_start + min(n_new, a + TPT) - 1) / kPN + 1;
+  };
+  const int n_tiles = max(tiles_of(qt), tiles_of(rank == 0 ? qt - 1 : qt + 1));
+  if (n_tiles == 0) return;                           // neither CTA holds a token
+  const int i0 = qt * TPT;
+  const int i1 = max(i0, min(n_new, i0 + TPT));       // i1 == i0: no rows of this CTA
   const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
 
   if (warp == 9) {
@@ -348,11 +391,11 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     *abort_flag = 0;
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], 2);   // released by both CTAs' MMAs
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], 2);
     }
     for (int s = 0; s < kSBufs; ++s) {
       mbar_init(&s_full[s], 1);
@@ -361,10 +404,12 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     }
     mbar_init(q_ready, kSoftmax);
     mbar_init(mma_idle, 1);
+    mbar_init(pv_idle, 1);
     fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any multicast write or remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_o = tmem + kOCol;
@@ -525,46 +570,56 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     // ============================ TMA producer ============================
     const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by the other query tiles
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    // cache row of this lane's block of key tile j (a block past the context,
-    // or a bad id, is read from rows outside the tensor, which TMA fills with zeros)
-    auto tile_row = [&](int j) -> int {
-      int id = -1;
-      if (lane < kPN / kBlockSize) {
-        const int blk = j * (kPN / kBlockSize) + lane;
-        id = (blk < nblk) ? row[blk] : -1;
-        if (blk < nblk && (id < 0 || id >= p.num_blocks)) {
-          record_error(p.err, PKV_ERR_OOB);
-          id = -1;
-        }
+    // block id of this lane's block of key tile j (-1 past the context), and
+    // its cache row: a block past the context, or a bad id, is read from rows
+    // outside the tensor, which TMA fills with zeros
+    auto fetch_id = [&](int j) -> int {
+      const int blk = j * (kPN / kBlockSize) + lane;
+      return (lane < kPN / kBlockSize && blk < nblk) ? row[blk] : -1;
+    };
+    auto to_row = [&](int j, int id) -> int {
+      const int blk = j * (kPN / kBlockSize) + lane;
+      if (lane < kPN / kBlockSize && blk < nblk && (id < 0 || id >= p.num_blocks)) {
+        record_error(p.err, PKV_ERR_OOB);
+        id = -1;
       }
       return (id >= 0) ? (id * p.n_kv_heads + g) * kBlockSize : -2 * kBlockSize;
     };
-    // load K (is_v = 0) or V of key tile j into its ring stage, after the
-    // stage's previous tile has been consumed
+    // load K (is_v = 0) or V of key tile j into its ring stage from cache row
+    // y, after the stage's previous tile has been consumed
     int issued_k = 0, issued_v = 0;
-    auto load = [&](int j, bool is_v) -> bool {
+    auto load = [&](int j, bool is_v, int y) -> bool {
       const int stages = is_v ? kVStages : kKStages;
       const int s = j % stages;
       uint64_t* full = is_v ? &v_full[s] : &k_full[s];
       uint64_t* empty = is_v ? &v_empty[s] : &k_empty[s];
       if (j >= stages && !__all_sync(0xffffffffu, mbar_wait(empty, ((j / stages) - 1) & 1, p.err))) return false;
-      const int y = tile_row(j);
+      // the whole tile lands in this CTA: its own half and the peer's
       if (lane == 0) mbar_arrive_expect_tx(full, kTile);
       __syncwarp();
-      if (lane < kPN / kBlockSize) {
+      if (lane < kPN / kBlockSize && (lane >> 2) == rank) {
         unsigned char* dst = sm + (is_v ? kOffV : kOffK) + s * kTile + lane * 2048;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          tma_load_2d(dst + h * (kTile / 2), is_v ? &p.tmap_v : &p.tmap_k, h * 64, y, full, pol);
+          tma_load_2d_pair(dst + h * (kTile / 2), is_v ? &p.tmap_v : &p.tmap_k, h * 64, y, full, pol);
       }
       __syncwarp();
       (is_v ? issued_v : issued_k) = j + 1;
       return true;
     };
-    // the order the MMAs consume them in: K0, K1, then V of tile j and K of tile j + 2
-    bool good = load(0, false) && (n_tiles < 2 || load(1, false));
+    // the order the MMAs consume them in: K0, K1, then V of tile j and K of
+    // tile j + 2.  Block ids are fetched a tile ahead of their first use (r0,
+    // r1 rows of tiles j, j + 1; id2 the raw id of tile j + 2), so the table's
+    // latency is spent while the ring waits.
+    int r0 = to_row(0, fetch_id(0)), r1 = (n_tiles > 1) ? to_row(1, fetch_id(1)) : 0;
+    int id2 = (n_tiles > 2) ? fetch_id(2) : -1;
+    bool good = load(0, false, r0) && (n_tiles < 2 || load(1, false, r1));
     for (int j = 0; good && j < n_tiles && !*abort_flag; ++j) {
-      good = load(j, true) && (j + 2 >= n_tiles || load(j + 2, false));
+      const int r2 = (j + 2 < n_tiles) ? to_row(j + 2, id2) : 0;
+      if (j + 3 < n_tiles) id2 = fetch_id(j + 3);
+      good = load(j, true, r0) && (j + 2 >= n_tiles || load(j + 2, false, r2));
+      r0 = r1;
+      r1 = r2;
     }
     if (!good) *abort_flag = 1;
     if (*abort_flag && lane == 0) {
@@ -576,102 +631,95 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
         mbar_wait_until(&v_full[jj % kVStages], (jj / kVStages) & 1, deadline);
     }
   } else {
-    // ============================ MMA issuer (warp 9) ============================
-    // One elected lane waits, issues and commits.  A tcgen05.commit holds its
-    // thread until the MMA queue ahead of the tensor cores has drained to a few
-    // MMAs, so each batch is committed at once and the next one's waits are
-    // short (their phases have completed by then).
-    const uint32_t sq = smem_u32(sm + kOffQ);
+    // ============================ MMA issuers (warps 9, 10) ============================
+    // Warp 9 issues Q K^T, warp 10 P V, one elected lane each.  A commit holds
+    // its thread until the MMA queue ahead of the tensor cores has drained to a
+    // few MMAs; with two issuing threads one of them can feed the queue while
+    // the other is held, and neither waits for the other's batches.
     constexpr int kPasses = kSplit ? 2 : 1;   // P_hi, then P_lo
     constexpr uint32_t kIdQK = umma_idesc<QT>(false), kIdPV = umma_idesc<QT>(true);
+    const bool qk_warp = (warp == 9);
+    uint64_t* idle = qk_warp ? mma_idle : pv_idle;
     bool ok = true;
-    if (lane == 0) ok = mbar_wait(q_ready, 0, p.err);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    // S = Q K^T of tile j into S buffer j % 3 (its previous tile's P V has
-    // completed: checked by the caller)
-    auto issue_qk = [&](int j) -> bool {
-      const int s = j % kKStages;
-      bool good = true;
-      if (lane == 0) good = mbar_wait(&k_full[s], (j / kKStages) & 1, p.err);
-      good = __shfl_sync(0xffffffffu, good, 0);
-      if (good && lane == 0) {
-        // descriptors built once per tile; each k-step adds a compile-time
-        // offset to the address field (addr >> 4, no carry out of its 14 bits
-        // for shared addresses below 256 KiB)
-        const uint64_t a0 = umma_desc(sq, 16, 1024), b0 = umma_desc(smem_u32(sm + kOffK + s * kTile), 16, 1024);
-        const uint32_t d = t_s(j);
-        tc_fence_after();
+    if (qk_warp) {
+      const uint32_t sq = smem_u32(sm + kOffQ);
+      if (lane == 0) ok = mbar_wait(q_ready, 0, p.err);
+      // S = Q K^T of tile t into S buffer t % 3, once the P V of tile t - 3
+      // (which read P from that buffer) has completed
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % kKStages;
+        if (lane == 0) {
+          ok = (t < kSBufs || mbar_wait(&pv_done[(t - kSBufs) % kSBufs], ((t - kSBufs) / kSBufs) & 1, p.err)) &&
+               mbar_wait(&k_full[s], (t / kKStages) & 1, p.err) && !*abort_flag;
+          if (ok) {
+            // descriptors built once per tile; each k-step adds a compile-time
+            // offset to the address field (addr >> 4, no carry out of its 14
+            // bits for shared addresses below 256 KiB)
+            const uint64_t a0 = umma_desc(sq, 16, 1024), b0 = umma_desc(smem_u32(sm + kOffK + s * kTile), 16, 1024);
+            const uint32_t d = t_s(t);
+            tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kPD / 16; ++ks) {
-          const uint64_t koff = static_cast<uint64_t>(((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4);
-          umma_f16(d, a0 + koff, b0 + koff, kIdQK, ks > 0);
+            for (int ks = 0; ks < kPD / 16; ++ks) {
+              const uint64_t koff = static_cast<uint64_t>(((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4);
+              umma_f16(d, a0 + koff, b0 + koff, kIdQK, ks > 0);
+            }
+            umma_commit(&s_full[t % kSBufs]);
+            umma_commit_pair(&k_empty[s]);
+          }
         }
-        umma_commit(&s_full[j % kSBufs]);
-        umma_commit(&k_empty[s]);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      __syncwarp();
-      return good;
-    };
-    if (ok && n_tiles > 0) ok = issue_qk(0);
-    if (ok && n_tiles > 1) ok = issue_qk(1);
-    for (int j = 0; j < n_tiles && ok && !*abort_flag; ++j) {
-      const int buf = j % kSBufs, vs = j % kVStages;
-      const uint32_t sv = smem_u32(sm + kOffV + vs * kTile);
-      if (lane == 0)
-        ok = mbar_wait(&p_full[buf], (j / kSBufs) & 1, p.err) && mbar_wait(&v_full[vs], (j / kVStages) & 1, p.err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      // the tile holding the context's last, partial block: its rows past the
-      // context have zero probability but may hold any bits; clear them in V
-      const int tail = ctx % kBlockSize;
-      if (tail != 0 && (nblk - 1) / (kPN / kBlockSize) == j) {
-        const int slot = (nblk - 1) % (kPN / kBlockSize);
-        for (int x = lane; x < (kBlockSize - tail) * 16; x += 32) {
-          const int rr = slot * kBlockSize + tail + x / 16, c = x % 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sv + tile_off(rr, c)), "r"(0u) : "memory");
+    } else {
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int buf = j % kSBufs, vs = j % kVStages;
+        const uint32_t sv = smem_u32(sm + kOffV + vs * kTile);
+        if (lane == 0)
+          ok = mbar_wait(&p_full[buf], (j / kSBufs) & 1, p.err) && mbar_wait(&v_full[vs], (j / kVStages) & 1, p.err) &&
+               !*abort_flag;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // the tile holding the context's last, partial block: its rows past the
+        // context have zero probability but may hold any bits; clear them in V
+        const int tail = ctx % kBlockSize;
+        if (tail != 0 && (nblk - 1) / (kPN / kBlockSize) == j) {
+          const int slot = (nblk - 1) % (kPN / kBlockSize);
+          for (int x = lane; x < (kBlockSize - tail) * 16; x += 32) {
+            const int rr = slot * kBlockSize + tail + x / 16, c = x % 16;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sv + tile_off(rr, c)), "r"(0u) : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
         }
-        fence_proxy_async_smem();
+        if (lane == 0) {
+          tc_fence_after();
+          // k-step ks takes keys 16 ks .. 16 ks + 15: chunk ks / 2, columns
+          // 8 (ks % 2) of its P_hi half (pass 0) or P_lo half (pass 1)
+          const uint64_t b0 = umma_desc(sv, kTile / 2, 1024);
+          const uint32_t a0 = t_s(j);
+#pragma unroll
+          for (int pass = 0; pass < kPasses; ++pass)
+#pragma unroll
+            for (int ks = 0; ks < kPN / 16; ++ks)
+              umma_f16_tmem_a(t_o, a0 + 32 * (ks >> 1) + 16 * pass + 8 * (ks & 1),
+                              b0 + static_cast<uint64_t>((ks * 2048) >> 4), kIdPV, j > 0 || ks > 0 || pass > 0);
+          umma_commit(&pv_done[buf]);
+          umma_commit_pair(&v_empty[vs]);
+        }
         __syncwarp();
-      }
-      if (lane == 0) {
-        tc_fence_after();
-        // k-step ks takes keys 16 ks .. 16 ks + 15: chunk ks / 2, columns
-        // 8 (ks % 2) of its P_hi half (pass 0) or P_lo half (pass 1)
-        const uint64_t b0 = umma_desc(sv, kTile / 2, 1024);
-        const uint32_t a0 = t_s(j);
-#pragma unroll
-        for (int pass = 0; pass < kPasses; ++pass)
-#pragma unroll
-          for (int ks = 0; ks < kPN / 16; ++ks)
-            umma_f16_tmem_a(t_o, a0 + 32 * (ks >> 1) + 16 * pass + 8 * (ks & 1),
-                            b0 + static_cast<uint64_t>((ks * 2048) >> 4), kIdPV, j > 0 || ks > 0 || pass > 0);
-        umma_commit(&pv_done[buf]);
-        umma_commit(&v_empty[vs]);
-      }
-      __syncwarp();
-      // S of tile j + 2 goes to the buffer of tile j - 1, free once its P V is done
-      if (j + 2 < n_tiles) {
-        if (j >= 1) {
-          if (lane == 0) ok = mbar_wait(&pv_done[(j - 1) % kSBufs], ((j - 1) / kSBufs) & 1, p.err);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-        }
-        if (!issue_qk(j + 2)) {
-          ok = false;
-          break;
-        }
       }
     }
     if (!ok) *abort_flag = 1;
-    // every MMA this thread issued has completed before TMEM is released
+    // every MMA this lane issued has completed before TMEM is released
     if (lane == 0) {
-      umma_commit(mma_idle);
-      mbar_wait(mma_idle, 0, p.err);
+      umma_commit(idle);
+      mbar_wait(idle, 0, p.err);
     }
     __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
+  // no multicast write or remote arrive of the peer is still in flight to this CTA
+  cluster_sync();
   tc_fence_after();
   if (warp == 9)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -695,11 +743,25 @@ pkv_status launch_prefill(PrefillParams& p, int q_tiles, cudaStream_t stream) {
       done[dev] = true;
     }
   }
-  const dim3 grid(static_cast<unsigned>(q_tiles), static_cast<unsigned>(p.n_kv_heads),
+  // clusters of two CTAs along the query tiles (an even count), launched
+  // with programmatic dependent launch like the other kernels
+  const dim3 grid(static_cast<unsigned>((q_tiles + 1) & ~1), static_cast<unsigned>(p.n_kv_heads),
                   static_cast<unsigned>(p.batch));
-  return cuda_failed(launch_pdl(kern, grid, dim3(kPThreads), kPrefillSmem, stream, p), "paged_prefill_kernel launch")
-             ? PKV_ERR_CUDA
-             : PKV_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPrefillSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cuda_failed(cudaLaunchKernelEx(&cfg, kern, p), "paged_prefill_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }
 
 template <typename QT>
