@@ -81,16 +81,18 @@ constexpr int kTile = kPM * kPD * 2;      // bytes of a 128 x 128 16-bit tile (Q
 constexpr int kPThreads = 352;           // 8 softmax warps, 1 TMA warp, 2 MMA warps
 constexpr int kSoftmax = 256;            // softmax threads: 2 per query row
 constexpr int kSBufs = 3;                 // S / P buffers in TMEM
-constexpr int kKStages = 3, kVStages = 2; // K and V rings in shared memory
+constexpr int kKStages = 2, kVStages = 3; // K and V rings in shared memory
 constexpr int kTmemCols = 512;            // S / P buffers at columns 0, 128, 256; O at 384
 constexpr int kOCol = kSBufs * kPN;
 constexpr float kRescaleLog2 = 8.f;      // the row reference moves when the max outgrows it by > 2^8
 
-// offsets in the 1024-aligned shared block: Q | K x 3 | V x 2 | barriers | row exchange
+// offsets in the 1024-aligned shared block: Q | K ring | V ring | barriers | row exchange
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;                          // stage s at kOffK + s kTile
 constexpr int kOffV = kOffK + kKStages * kTile;       // stage s at kOffV + s kTile
 constexpr int kOffBar = kOffV + kVStages * kTile;
+constexpr int kBarWords = 2 * (kKStages + kVStages) + 3 * kSBufs + 3 + 2;   // barriers, TMEM slot, abort flag
+static_assert(kBarWords * 8 <= 256, "barrier block overflows its 256 bytes");
 constexpr int kOffRed = kOffBar + 256;                // float [3][2][128]: row maxima (2 slots), row sums
 constexpr size_t kPrefillSmem = static_cast<size_t>(kOffRed) + 3 * 2 * kPM * 4 + 1024;
 
@@ -338,18 +340,19 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
   extern __shared__ unsigned char psm_raw[];
   unsigned char* sm = psm_raw + ((1024 - (smem_u32(psm_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint64_t* k_full = bars;                 // [3] K of the stage's tile landed
-  uint64_t* k_empty = bars + 3;            // [3] Q K^T of the stage's tile done: K may be reloaded
-  uint64_t* v_full = bars + 6;             // [2] V landed
-  uint64_t* v_empty = bars + 8;            // [2] P V done: V may be reloaded
-  uint64_t* s_full = bars + 10;            // [3] per S / P buffer: scores ready
-  uint64_t* p_full = bars + 13;            // [3] per buffer, kSoftmax arrivals: P written, O rescaled
-  uint64_t* pv_done = bars + 16;           // [3] per buffer: P V of its tile done
-  uint64_t* q_ready = bars + 19;           // kSoftmax arrivals
-  uint64_t* mma_idle = bars + 20;          // Q K^T issuer drained
-  uint64_t* pv_idle = bars + 21;           // P V issuer drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 23);
+  // barrier array offsets follow the ring sizes (kBarWords words in all)
+  uint64_t* k_full = bars;                    // [kKStages] K of the stage's tile landed
+  uint64_t* k_empty = k_full + kKStages;      // [kKStages] Q K^T of the stage's tile done in both CTAs
+  uint64_t* v_full = k_empty + kKStages;      // [kVStages] V landed
+  uint64_t* v_empty = v_full + kVStages;      // [kVStages] P V done in both CTAs
+  uint64_t* s_full = v_empty + kVStages;      // [3] per S / P buffer: scores ready
+  uint64_t* p_full = s_full + kSBufs;         // [3] per buffer, kSoftmax arrivals: P written, O rescaled
+  uint64_t* pv_done = p_full + kSBufs;        // [3] per buffer: P V of its tile done
+  uint64_t* q_ready = pv_done + kSBufs;       // kSoftmax arrivals
+  uint64_t* mma_idle = q_ready + 1;           // Q K^T issuer drained
+  uint64_t* pv_idle = mma_idle + 1;           // P V issuer drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_idle + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(pv_idle + 2);
   float* red = reinterpret_cast<float*>(sm + kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
