@@ -81,6 +81,7 @@ constexpr int kTile = kPM * kPD * 2;      // bytes of a 128 x 128 16-bit tile (Q
 constexpr int kPThreads = 352;           // 8 softmax warps, 1 TMA warp, 2 MMA warps
 constexpr int kSoftmax = 256;            // softmax threads: 2 per query row
 constexpr int kSBufs = 3;                 // S / P buffers in TMEM
+constexpr int kCluster = 2;               // CTAs (adjacent query tiles) sharing each K / V tile load
 constexpr int kKStages = 2, kVStages = 3; // K and V rings in shared memory
 constexpr int kTmemCols = 512;            // S / P buffers at columns 0, 128, 256; O at 384
 constexpr int kOCol = kSBufs * kPN;
@@ -146,18 +147,19 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
-      "h"(static_cast<uint16_t>(3))
+      "h"(static_cast<uint16_t>((1u << kCluster) - 1))
       : "memory");
 }
 
-// tiled TMA load written to the same shared offset of both CTAs of the cluster,
+// tiled TMA load written to the same shared offset of every CTA of the cluster,
 // completing on the barrier at `bar`'s offset in each
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                                  uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint "
       "[%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+      "h"(static_cast<uint16_t>((1u << kCluster) - 1)),
       "l"(policy)
       : "memory");
 }
@@ -378,7 +380,8 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     const int a = qtile * TPT;
     return (qtile < 0 || a >= n_new) ? 0 : (q_start + min(n_new, a + TPT) - 1) / kPN + 1;
   };
-  const int n_tiles = max(tiles_of(qt), tiles_of(rank == 0 ? qt - 1 : qt + 1));
+  int n_tiles = 0;   // the longest query tile of the cluster: rank r holds qt = qt_of_rank_0 - r
+  for (int r = 0; r < kCluster; ++r) n_tiles = max(n_tiles, tiles_of(qt + rank - r));
   if (n_tiles == 0) return;                           // neither CTA holds a token
   const int i0 = qt * TPT;
   const int i1 = max(i0, min(n_new, i0 + TPT));       // i1 == i0: no rows of this CTA
@@ -394,11 +397,11 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
     *abort_flag = 0;
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 2);   // released by both CTAs' MMAs
+      mbar_init(&k_empty[s], kCluster);   // released by every CTA's MMAs
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 2);
+      mbar_init(&v_empty[s], kCluster);
     }
     for (int s = 0; s < kSBufs; ++s) {
       mbar_init(&s_full[s], 1);
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(kPThreads, 1) paged_prefill_kernel(const __gri
       // the whole tile lands in this CTA: its own half and the peer's
       if (lane == 0) mbar_arrive_expect_tx(full, kTile);
       __syncwarp();
-      if (lane < kPN / kBlockSize && (lane >> 2) == rank) {
+      if (lane < kPN / kBlockSize && lane / (kPN / kBlockSize / kCluster) == rank) {
         unsigned char* dst = sm + (is_v ? kOffV : kOffK) + s * kTile + lane * 2048;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -748,7 +751,7 @@ pkv_status launch_prefill(PrefillParams& p, int q_tiles, cudaStream_t stream) {
   }
   // clusters of two CTAs along the query tiles (an even count), launched
   // with programmatic dependent launch like the other kernels
-  const dim3 grid(static_cast<unsigned>((q_tiles + 1) & ~1), static_cast<unsigned>(p.n_kv_heads),
+  const dim3 grid(static_cast<unsigned>((q_tiles + kCluster - 1) / kCluster * kCluster), static_cast<unsigned>(p.n_kv_heads),
                   static_cast<unsigned>(p.batch));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -759,7 +762,7 @@ pkv_status launch_prefill(PrefillParams& p, int q_tiles, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.x = kCluster;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
