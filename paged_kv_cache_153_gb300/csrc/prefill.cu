@@ -41,11 +41,21 @@
 // exceeds it by more than 2^8 (P stays <= 256, exact in fp32 accumulation):
 // only then is the O row rescaled, after the previous P V has completed, so
 // in the steady state the softmax never waits for the tensor cores.
-// Warp roles: warps 0-7 softmax and epilogue, warp 8 TMA producer (K in a
-// 3-stage ring, V in a 2-stage ring, issued in the order the MMAs consume
-// them: V of tile j, then K of tile j + 2), warp 9 TMEM owner and MMA issuer
-// (one elected lane).  Every wait is bounded; on expiry the block records
-// PKV_ERR_TIMEOUT, drains what it has in flight and frees its TMEM.
+// Loads.  A TMA load of one 16-row block moves only about 25 B per clock per
+// SM on GB300 (small boxes are request-bound), short of the ~42 B/clk the
+// tensor cores consume here, so CTAs run in clusters of two that hold
+// adjacent query tiles of the same (sequence, KV head): each loads half of the
+// blocks of every K / V tile with multicast into both, and a ring stage is
+// released by both CTAs' MMA commits (multicast to both).  Both run the key
+// tiles of the longer query tile; the other's rows see the extra keys masked.
+// Warp roles: warps 0-7 softmax and epilogue; warp 8 TMA producer (K in a
+// 2-stage ring, V in a 3-stage one, issued in the order the MMAs consume
+// them: V of tile j, then K of tile j + 2, with block-table entries read a
+// tile ahead); warp 9 TMEM owner and Q K^T issuer, warp 10 P V issuer (one
+// elected lane each: a commit holds its thread until the MMA queue has
+// drained to a few entries, so two issuers keep the queue fed).  Every wait
+// is bounded; on expiry the block records PKV_ERR_TIMEOUT, drains what it
+// has in flight and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
