@@ -100,15 +100,38 @@ __global__ void __launch_bounds__(kQThreads) quantize_int8_kernel(const void* k_
   if (threadIdx.x == 0) params[slab] = make_float4(lohi[0], lohi[1], lohi[2], lohi[3]);
 }
 
+// min and max over one half of the block (128 threads, 4 warps, named barrier
+// 1 + half); NaN-free inputs
+__device__ __forceinline__ float2 half_minmax(float lo, float hi, float2* scratch, int half) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, m));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, m));
+  }
+  const int w = (threadIdx.x >> 5) & 3;
+  if ((threadIdx.x & 31) == 0) scratch[4 * half + w] = make_float2(lo, hi);
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
+  float2 r = scratch[4 * half];
+#pragma unroll
+  for (int k = 1; k < 4; ++k) {
+    r.x = fminf(r.x, scratch[4 * half + k].x);
+    r.y = fmaxf(r.y, scratch[4 * half + k].y);
+  }
+  return r;
+}
+
 // one thread block per (token, KV head): write the token's row and re-quantise
-// rows [0, row] of its block's K and V slabs
+// rows [0, row] of its block's K slab (threads 0-127) and V slab (128-255)
+// side by side
 template <typename IN>
 __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_new, const void* v_new,
                                                                 const int64_t* slots, uint8_t* k_codes,
                                                                 uint8_t* v_codes, float4* params,
                                                                 int64_t num_slots, int n_heads, int d,
                                                                 int32_t* err) {
-  __shared__ float2 scratch[kQThreads / 32];
+  constexpr int kPer = 2 * kQPer;   // values per thread: 16 rows x 128 / 128
+  __shared__ float2 scratch[8];
+  __shared__ float2 lohi_out[2];
   pdl_wait_and_release();
   const int64_t t = blockIdx.x / n_heads;
   const int h = static_cast<int>(blockIdx.x % n_heads);
@@ -118,40 +141,46 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
     if (threadIdx.x == 0) record_error(err, PKV_ERR_OOB);
     return;
   }
+  const int which = threadIdx.x >> 7;   // 0: K, 1: V
+  const int ht = threadIdx.x & 127;
   const int64_t slab = (s / kBlockSize) * n_heads + h;
   const int row = static_cast<int>(s % kBlockSize);
   const int count = (row + 1) * d;
-  float4 prm = params[slab];
-  float out_lohi[4];
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    uint8_t* codes = (which ? v_codes : k_codes) + slab * kBlockSize * d;
-    const float lo_old = which ? prm.z : prm.x, hi_old = which ? prm.w : prm.y;
-    const void* src = which ? v_new : k_new;
-    float x[kQPer];
-    float lo = INFINITY, hi = -INFINITY;
+  const float4 prm = params[slab];
+  uint8_t* codes = (which ? v_codes : k_codes) + slab * kBlockSize * d;
+  const float lo_old = which ? prm.z : prm.x, hi_old = which ? prm.w : prm.y;
+  const void* src = which ? v_new : k_new;
+  uint8_t q[kPer];
 #pragma unroll
-    for (int k = 0; k < kQPer; ++k) {
-      const int i = threadIdx.x + k * kQThreads;
-      x[k] = 0.f;
-      if (i < count) {
-        x[k] = (i >= row * d) ? in_f32(src, (t * n_heads + h) * d + (i - row * d), IN{})
-                              : int8_decode_f32(codes[i], lo_old, hi_old);
-        lo = fminf(lo, x[k]);
-        hi = fmaxf(hi, x[k]);
-      }
-    }
-    const float2 mm = block_minmax(lo, hi, scratch);   // (its barriers order every read before the writes)
-    const float span = __fsub_rn(mm.y, mm.x);
-#pragma unroll
-    for (int k = 0; k < kQPer; ++k) {
-      const int i = threadIdx.x + k * kQThreads;
-      if (i < count) codes[i] = int8_code(x[k], mm.x, span);
-    }
-    out_lohi[2 * which] = mm.x;
-    out_lohi[2 * which + 1] = mm.y;
+  for (int k = 0; k < kPer; ++k) {
+    const int i = ht + k * 128;
+    q[k] = (i < row * d) ? codes[i] : 0;
   }
-  if (threadIdx.x == 0) params[slab] = make_float4(out_lohi[0], out_lohi[1], out_lohi[2], out_lohi[3]);
+  float x[kPer];
+  float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = ht + k * 128;
+    x[k] = 0.f;
+    if (i < count) {
+      x[k] = (i >= row * d) ? in_f32(src, (t * n_heads + h) * d + (i - row * d), IN{})
+                            : int8_decode_f32(q[k], lo_old, hi_old);
+      lo = fminf(lo, x[k]);
+      hi = fmaxf(hi, x[k]);
+    }
+  }
+  // (the named barrier inside orders every read of the half's codes before its writes)
+  const float2 mm = half_minmax(lo, hi, scratch, which);
+  const float span = __fsub_rn(mm.y, mm.x);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = ht + k * 128;
+    if (i < count) codes[i] = int8_code(x[k], mm.x, span);
+  }
+  if (ht == 0) lohi_out[which] = mm;
+  __syncthreads();
+  if (threadIdx.x == 0)
+    params[slab] = make_float4(lohi_out[0].x, lohi_out[0].y, lohi_out[1].x, lohi_out[1].y);
 }
 
 }  // namespace pkv
