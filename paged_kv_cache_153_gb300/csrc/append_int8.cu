@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
       hi = fmaxf(hi, x[k]);
     }
   }
-  // (the named barrier inside orders every read of the half's codes before its writes)
+  // (each thread rewrites only the codes it read, so no barrier is needed
+  // between the reads and the writes)
   const float2 mm = half_minmax(lo, hi, scratch, which);
   const float span = __fsub_rn(mm.y, mm.x);
 #pragma unroll
