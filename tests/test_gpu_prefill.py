@@ -121,3 +121,17 @@ def test_full_size_sampled(pkv):
     rows = sorted(set(rng.integers(0, pi.q.shape[0], 48).tolist()) |
                   {0, 127, 128, 2047, 2048, int(pi.q.shape[0]) - 1})
     _compare(out, _oracle(pi, rows=rows), rows=rows)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_cluster_pairs(pkv, dtype):
+    # Query tiles run in pairs that share K/V loads.  At G = 4 (32 tokens per
+    # tile): a pair whose tiles need 3 and 4 key tiles (positions 350..381 and
+    # 382..413), a pair with one empty tile (33 new tokens: tiles 0 and 1 with
+    # one token), a single tile padded with an empty partner (32 new tokens),
+    # and a one-token decode row.
+    pi = wl.prefill_inputs("pairs", cached_lens=[350, 0, 17, 4000], new_lens=[64, 33, 32, 1], n_q_heads=16,
+                           n_kv_heads=4, head_dim=128, dtype=dtype, seed=21)
+    out, err = _run(pkv, pi)
+    assert err == 0
+    _compare(out, _oracle(pi))
