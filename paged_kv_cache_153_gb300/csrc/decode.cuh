@@ -276,14 +276,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   return r;
 }
 // two one-byte codes (bits 0-15 of w) -> packed f16x2, exactly: E4M3 values,
-// or INT8 codes as integers (0x64cc is 1024 + cc in f16; subtracting 1024 is exact)
+// or INT8 codes offset by 1024 (0x64cc is 1024 + cc in f16, one byte permute;
+// the consumer folds the offset into its per-block affine terms)
 __device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, E4M3) { return e4m3x2_to_f16x2(w); }
-__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, U8) {
-  const uint32_t r = __byte_perm(w, 0x64u, 0x4140u);
-  uint32_t out;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(r), "r"(0x64006400u));
-  return out;
-}
+__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, U8) { return __byte_perm(w, 0x64u, 0x4140u); }
 
 
 // address of 16-byte chunk `chunk` of row `row` in a slab staged as 128B-swizzled
@@ -737,8 +733,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty_bar[qs]);
-      // INT8 cache: the MMAs see the codes as integers; a score is
-      // dk (q . codes) + k_min sum(q) and p . V is dv (p . codes) + v_min sum(p)
+      // INT8 cache: the MMAs see the codes as integers offset by 1024; a
+      // score is dk (q . codes) + k_min sum(q) and p . V is
+      // dv (p . codes) + v_min sum(p), the offset taken out of both sums
       constexpr bool kInt8 = T::kParam > 0;
       float qs0 = 0.f, qs1 = 0.f, b0r = 0.f, b1r = 0.f;   // sum(q) of heads h0, h0 + 1; v_min sum(p)
       if constexpr (kInt8) {
@@ -805,13 +802,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         if constexpr (kInt8) {
           const float4 prm = n_valid > 0 ? *reinterpret_cast<const float4*>(smem + T::prm_off(S) + s * T::kParam)
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          // the MMAs saw 1024 + code: dk (q . (1024 + codes)) + (k_min - 1024 dk) sum(q)
           const float dk = (prm.y - prm.x) * (1.f / 255.f);
           dv = (prm.w - prm.z) * (1.f / 255.f);
           vmin = prm.z;
-          c[0] = fmaf(c[0], dk, prm.x * qs0);
-          c[1] = fmaf(c[1], dk, prm.x * qs1);
-          c[2] = fmaf(c[2], dk, prm.x * qs0);
-          c[3] = fmaf(c[3], dk, prm.x * qs1);
+          const float kmin = prm.x - 1024.f * dk;
+          c[0] = fmaf(c[0], dk, kmin * qs0);
+          c[1] = fmaf(c[1], dk, kmin * qs1);
+          c[2] = fmaf(c[2], dk, kmin * qs0);
+          c[3] = fmaf(c[3], dk, kmin * qs1);
         }
         const bool v0 = r4 < n_valid, v1 = r4 + 8 < n_valid;
         const float s00 = v0 ? c[0] * sc : -INFINITY, s01 = v0 ? c[1] * sc : -INFINITY;
@@ -850,8 +849,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         l0 = l0 * a0 + ((p0.x + r0.x) + (p1.x + r1.x));
         l1 = l1 * a1 + ((p0.y + r0.y) + (p1.y + r1.y));
         if constexpr (kInt8) {
-          b0r = b0r * a0 + (p0.x + p1.x) * vmin;
-          b1r = b1r * a1 + (p0.y + p1.y) * vmin;
+          // the MMA adds 1024 f16(p dv) per key on top of f16(p dv) code: take
+          // exactly that out (from the packed values), and add v_min sum(p)
+          const float2 u0 = unpack2(x0, MT{}), u1 = unpack2(x1, MT{});
+          b0r = b0r * a0 + ((p0.x + p1.x) * vmin - 1024.f * (u0.x + u1.x));
+          b1r = b1r * a1 + ((p0.y + p1.y) * vmin - 1024.f * (u0.y + u1.y));
         }
         const bool resc = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
         m0 = mn0;
