@@ -71,11 +71,6 @@ int env_int(const char* name, int fallback) {
 }
 
 constexpr int kMaxCtasPerSm = 4;   // partial slots are sized for this many blocks per SM
-// Cost of one (sequence, KV head) in the balanced split, in quarter blocks:
-// the per-segment work (query load, cross-warp merge, output or partial
-// write) and the consumer warps left idle by short segments.  Measured best
-// on GB300 at 24 (6 blocks' worth of streaming) for mixed context lengths.
-constexpr int kUnitCost = 24;
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -195,7 +190,8 @@ pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const 
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_nblk = (max_context_len + kBlockSize - 1) / kBlockSize;
   p.part_blocks = partition_tokens / kBlockSize;
-  p.unit_cost = std::max(0, std::min(1 << 16, env_int("PKV_UNIT_COST", kUnitCost)));
+  // (-1: the launched variant's default cost per (sequence, KV head))
+  p.unit_cost = std::max(-1, std::min(1 << 16, env_int("PKV_UNIT_COST", -1)));
   p.slot_capacity = static_cast<int>(w.slots);
   p.qk_scale_log2 = scale * kLog2e;
 

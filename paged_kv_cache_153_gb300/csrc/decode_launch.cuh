@@ -68,6 +68,13 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   // consumer warps; 3 for E4M3 through the tensor cores, whose per-block
   // conversions want more consumer warps.
   const int want = li.max_ctas_per_sm > 0 ? li.max_ctas_per_sm : ((MMA && Tr::kEsz == 1) ? 3 : 2);
+  // Cost of one (sequence, KV head) in the balanced split, in quarter blocks:
+  // the per-segment work (query load, cross-warp merge, output or partial
+  // write) and the consumer warps left idle by short segments.  Measured on
+  // GB300 with mixed context lengths: 24 (6 blocks' worth of streaming) for
+  // the CUDA-core consumer; 48 for the tensor-core one, whose per-segment
+  // set-up is larger (gqa8b 83.4 -> 82.0 us, INT8 60.9 -> 59.0 us against 24).
+  if (p.unit_cost < 0) p.unit_cost = MMA ? 48 : 24;
   occ = std::min(occ, want);
   int spw = 1;
   if (li.stages > 0) {
