@@ -355,9 +355,12 @@ void pkv_step_graph_destroy(pkv_step_graph* graph);
  * the caches [num_blocks, num_kv_heads, 16, 128] of the same dtype;
  * block_tables int32 [batch, max_blocks_per_seq]; context_lens, cu_seqlens
  * int32 device arrays; max_query_len >= every n_b.  Runs on the tensor cores
- * (tcgen05, accumulators in tensor memory) with fp32 softmax; P is rounded to
- * dtype before P.V.  head_dim 128 and block_size 16 only (else
- * PKV_ERR_UNSUPPORTED).  Device errors in err_flag: PKV_ERR_OOB for a block id
+ * (tcgen05, scores, P and accumulators in tensor memory) with fp32 softmax;
+ * fp16 P is rounded to fp16 before P.V, bf16 P is multiplied as a pair of
+ * bf16 parts (hi = p truncated, lo = p - hi rounded), exact to ~2^-16.  The
+ * kernel launches in clusters of two thread blocks that share each K/V tile
+ * load; a launch the device cannot schedule returns PKV_ERR_CUDA.  head_dim
+ * 128 and block_size 16 only (else PKV_ERR_UNSUPPORTED).  Device errors in err_flag: PKV_ERR_OOB for a block id
  * outside [0, num_blocks), more new tokens than context or a context past the
  * table (that sequence's tile is skipped); PKV_ERR_TIMEOUT if a pipeline wait
  * exceeds its limit.
