@@ -135,3 +135,13 @@ def test_cluster_pairs(pkv, dtype):
     out, err = _run(pkv, pi)
     assert err == 0
     _compare(out, _oracle(pi))
+
+
+def test_sequences_without_new_tokens(pkv):
+    # a sequence with no new tokens (equal cu_seqlens entries) has no rows and
+    # no query tile; the others are unaffected
+    pi = wl.prefill_inputs("zero-new", cached_lens=[30, 64, 5, 200], new_lens=[0, 17, 0, 90], n_q_heads=16,
+                           n_kv_heads=4, head_dim=128, dtype="bf16", seed=33)
+    out, err = _run(pkv, pi)
+    assert err == 0
+    _compare(out, _oracle(pi))
