@@ -846,6 +846,9 @@ def run_prefill(args, rank: int, local_rank: int) -> dict | None:
     }
 
 
+SINGLE_GPU_WORKLOADS = ("prefill", "cow", "int8", "layers")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -860,6 +863,18 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    # Single-GPU workloads: refused under torchrun before any CUDA call.  The
+    # prefill kernel's clusters share K/V tiles by TMA multicast, which is for
+    # single-GPU processes only; the others have no replica path.
+    if world > 1 and args.workload in SINGLE_GPU_WORKLOADS:
+        if rank == 0:
+            line = {"unavailable": f"--workload {args.workload} runs on one GPU only (world size {world} refused "
+                                   "before any CUDA call)"}
+            if args.impl == "reference":
+                line = {"impl": "reference", **line}
+            print(json.dumps(line), flush=True)
+        return
 
     if args.workload == "int8":
         if args.impl == "reference":

@@ -28,6 +28,7 @@ __all__ = [
 
 PKV_F16 = 0
 PKV_BF16 = 1
+PKV_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # as in pkv.h
 _DIR = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_DIR, "libpkv.so")
 
@@ -35,6 +36,23 @@ if not os.path.exists(library_path):
     raise ImportError(f"{library_path} is missing: build it with __graft_entry__.build() "
                       "(the CUDA path has no fallback)")
 lib = C.CDLL(library_path)
+
+# The prefill kernel lives in a library of its own (pkv_prefill.h), loaded on
+# first use, so that a process that only decodes never loads it.
+prefill_library_path = os.path.join(_DIR, "libpkv_prefill.so")
+_prefill_lib = None
+
+
+def prefill_lib():
+    global _prefill_lib
+    if _prefill_lib is None:
+        if not os.path.exists(prefill_library_path):
+            raise ImportError(f"{prefill_library_path} is missing: build it with __graft_entry__.build()")
+        pl = C.CDLL(prefill_library_path)
+        pl.pkv_paged_prefill_attention.restype = C.c_int
+        pl.pkv_paged_prefill_attention.argtypes = _PREFILL_SIG
+        _prefill_lib = pl
+    return _prefill_lib
 
 _p, _i, _i64, _sz, _f = C.c_void_p, C.c_int, C.c_int64, C.c_size_t, C.c_float
 _SIGS = {
@@ -68,8 +86,6 @@ _SIGS = {
     "pkv_pool_cow": (_i, [_p, C.c_int32, C.POINTER(C.c_int32)]),
     "pkv_prepare_append": (_i, [_p, _p, _i, _i, _p, _p, _p, C.POINTER(C.c_int32)]),
     "pkv_copy_blocks": (_i, [_p, _p, _i64, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
-    "pkv_paged_prefill_attention": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
-                                         _p, _p]),
     "pkv_paged_decode_step_layer": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _i, _i, _f,
                                          _p, _i, _i, _p, _p, _sz, _p, _p]),
     "pkv_step_graph_create": (_i, [C.POINTER(_p), _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
@@ -81,6 +97,7 @@ _SIGS = {
     "pkv_paged_decode_attention_int8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
                                              _i, _p, _sz, _p, _p]),
 }
+_PREFILL_SIG = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i, _p, _p]
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
     _fn.restype = _res
@@ -277,7 +294,7 @@ def pkv_paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens,
     """Causal extend attention of the new tokens q [T, Hq, D] over the paged
     cache (which already holds their K/V)."""
     nb, hkv, bs, d = k_cache.shape
-    _check("pkv_paged_prefill_attention", lib.pkv_paged_prefill_attention(
+    _check("pkv_paged_prefill_attention", prefill_lib().pkv_paged_prefill_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(cu_seqlens),
         context_lens.numel(), q.shape[1], hkv, d, bs, block_tables.shape[1], nb, max_query_len, scale, _ptr(out),
         _dtype_code(q, dtype), _ptr(err_flag), _stream(stream)))

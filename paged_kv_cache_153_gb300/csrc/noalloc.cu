@@ -9,9 +9,6 @@
 // until the process exits.  Nothing here allocates.
 #include <cuda_runtime.h>
 
-#include <cstdio>
-#include <mutex>
-
 #include "../../include/pkv.h"
 #include "host_util.h"
 
@@ -22,23 +19,15 @@ namespace {
 // device symbol; its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, resolved once per
-// device (the first call on a device does this set-up).
+// Device address of the scratch in the current device's context.  It is
+// looked up on every call (cudaGetSymbolAddress allocates nothing and, once
+// the module is loaded, is a host-side table lookup), so the address stays
+// right after a cudaDeviceReset or in another context of the same device.
+// The first call on a device loads the library's device code there.
 pkv_status scratch_on_current_device(void** out) {
-  int dev = 0;
-  if (cuda_failed(cudaGetDevice(&dev), "cudaGetDevice")) return PKV_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cuda_failed(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress")) return PKV_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cuda_failed(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress")) return PKV_ERR_CUDA;
+  *out = p;
   return PKV_OK;
 }
 
@@ -52,10 +41,12 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(const void* q, const vo
                                                          int64_t num_blocks, int max_context_len, float scale,
                                                          void* out, pkv_dtype dtype, int partition_tokens,
                                                          int32_t* err_flag, void* stream) {
-  if (batch == 0) return PKV_OK;
+  // Sizes beyond the scratch are refused before anything else.  A size of 0
+  // (arguments the query rejects, or a failed device query) falls through:
+  // the workspace entry point below validates in its own order and returns
+  // the same status it would return to a caller with a workspace.
   const size_t need = pkv_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                                  max_context_len, partition_tokens);
-  if (need == 0) return PKV_ERR_INVALID_ARG;
   if (need > PKV_NOALLOC_SCRATCH_BYTES) {
     // too large for the fixed scratch: refuse rather than overrun it
     pkv::cuda_failed(cudaErrorMemoryAllocation, "pkv_paged_decode_attention_noalloc: scratch too small");

@@ -62,6 +62,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "../../include/pkv_prefill.h"
 #include "host_util.h"
 #include "pkv_common.cuh"
 

@@ -21,22 +21,41 @@ def pkv():
     return m
 
 
-def declared_symbols():
+# each header and the library that exports what it declares
+HEADER_LIBRARIES = {"pkv.h": "libpkv.so", "pkv_prefill.h": "libpkv_prefill.so"}
+
+
+def declared_symbols(header=None):
     names = set()
     for fname in os.listdir(os.path.join(ROOT, "include")):
-        if fname.endswith(".h"):
+        if fname.endswith(".h") and (header is None or fname == header):
             text = open(os.path.join(ROOT, "include", fname)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
     return names
 
 
-def test_every_declared_symbol_is_exported(pkv):
-    names = declared_symbols()
-    assert {"pkv_kv_append", "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8"} <= names
-    lib = C.CDLL(pkv.library_path)
+def test_every_header_has_a_library():
+    headers = {f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")}
+    assert headers == set(HEADER_LIBRARIES)
+
+
+@pytest.mark.parametrize("header", sorted(HEADER_LIBRARIES))
+def test_every_declared_symbol_is_exported(pkv, header):
+    names = declared_symbols(header)
+    if header == "pkv.h":
+        assert {"pkv_kv_append", "pkv_paged_decode_attention", "pkv_paged_decode_attention_fp8"} <= names
+    else:
+        assert names == {"pkv_paged_prefill_attention"}
+    lib = C.CDLL(os.path.join(os.path.dirname(pkv.library_path), HEADER_LIBRARIES[header]))
     missing = [n for n in sorted(names) if not hasattr(lib, n)]
     assert not missing, missing
+
+
+def test_decode_library_holds_no_prefill_kernel(pkv):
+    # a decode-only process never loads the clustered prefill kernel
+    lib = C.CDLL(pkv.library_path)
+    assert not hasattr(lib, "pkv_paged_prefill_attention")
 
 
 def test_status_strings(pkv):
