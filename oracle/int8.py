@@ -31,17 +31,27 @@ import numpy as np
 F32 = np.float32
 
 
+def encode_slabs(values: np.ndarray):
+    """Codes (uint8, same shape) and per-slab (min, max) as float32 for a
+    stack of slabs ``values`` [..., rows, d] (every row holds a token): each
+    slab [rows, d] is encoded on its own with the formula above, its min and
+    max taken over that slab alone."""
+    x = np.asarray(values, dtype=F32)
+    lo = x.min(axis=(-2, -1), keepdims=True)
+    hi = x.max(axis=(-2, -1), keepdims=True)
+    span = (hi - lo).astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = ((x - lo) / span) * F32(255.0)      # float32 ops, left to right
+    q = np.clip(np.rint(t), 0, 255)
+    q = np.where(span == 0, 0, q).astype(np.uint8)
+    return q, lo[..., 0, 0], hi[..., 0, 0]
+
+
 def encode_rows(values: np.ndarray):
     """Codes [rows, d] (uint8) and (min, max) as float32 for the float32 rows
-    ``values`` (all of them hold tokens)."""
-    x = np.asarray(values, dtype=F32)
-    lo, hi = F32(x.min()), F32(x.max())
-    span = F32(hi - lo)
-    if span == 0:
-        return np.zeros(x.shape, dtype=np.uint8), lo, hi
-    t = ((x - lo) / span) * F32(255.0)          # float32 ops, left to right
-    q = np.clip(np.rint(t), 0, 255).astype(np.uint8)
-    return q, lo, hi
+    ``values`` (all of them hold tokens): one slab of ``encode_slabs``."""
+    q, lo, hi = encode_slabs(np.asarray(values, dtype=F32)[None])
+    return q[0], F32(lo[0]), F32(hi[0])
 
 
 def decode_f64(codes: np.ndarray, lo, hi) -> np.ndarray:
@@ -59,18 +69,24 @@ def decode_f32(codes: np.ndarray, lo, hi) -> np.ndarray:
 def quantize_pool(pool_f32: np.ndarray, rows_used=None):
     """Quantise a float32 pool [NB, H, 16, d]: codes [NB, H, 16, d] and
     params [NB, H, 2] (min, max).  rows_used[blk] (default 16) rows of each
-    block hold tokens; the rest get code 0."""
+    block hold tokens; the rest get code 0 (and a block with none gets
+    (0, 0)).  Blocks with the same number of used rows are encoded together
+    (slab by slab, as ``encode_slabs`` does)."""
     nb, nh, bs, d = pool_f32.shape
     codes = np.zeros(pool_f32.shape, dtype=np.uint8)
     params = np.zeros((nb, nh, 2), dtype=F32)
-    for blk in range(nb):
-        n = bs if rows_used is None else int(rows_used[blk])
+    used = np.full(nb, bs) if rows_used is None else np.asarray(rows_used).astype(np.int64)
+    for n in np.unique(used):
+        n = int(n)
         if n == 0:
             continue
-        for h in range(nh):
-            q, lo, hi = encode_rows(pool_f32[blk, h, :n])
-            codes[blk, h, :n] = q
-            params[blk, h] = (lo, hi)
+        blks = np.nonzero(used == n)[0]
+        for s in range(0, blks.size, 4096):    # bounded temporaries
+            part = blks[s:s + 4096]
+            q, lo, hi = encode_slabs(pool_f32[part, :, :n])
+            codes[part, :, :n] = q
+            params[part, :, 0] = lo
+            params[part, :, 1] = hi
     return codes, params
 
 

@@ -64,3 +64,48 @@ def test_pool_quantisation_leaves_unused_rows_zero():
     codes, params = oi.quantize_pool(pool, rows_used=[16, 5, 0])
     assert (codes[1, :, 5:] == 0).all() and (codes[2] == 0).all() and (params[2] == 0).all()
     assert params[1, 0, 0] == pool[1, 0, :5].min() and params[1, 0, 1] == pool[1, 0, :5].max()
+
+
+def test_worked_example_through_the_slab_encoder():
+    # the same worked example as one slab of a stack, next to a constant slab
+    x = np.array([[[-1.0, 0.0, 1.0]], [[2.5, 2.5, 2.5]]], dtype=np.float32)
+    q, lo, hi = oi.encode_slabs(x)
+    assert q.tolist() == [[[0, 128, 255]], [[0, 0, 0]]]
+    assert lo.tolist() == [-1.0, 2.5] and hi.tolist() == [1.0, 2.5]
+
+
+def test_each_slab_uses_only_its_own_range():
+    # slabs of very different ranges side by side: each slab's extremes map to
+    # 0 and 255 and its codes stay within half a step of its own values (a min
+    # or max taken over the wrong axes would break one of these)
+    rng = np.random.default_rng(11)
+    x = (rng.normal(size=(5, 3, 16, 32)) * np.array([0.01, 1.0, 100.0])[None, :, None, None]).astype(np.float32)
+    q, lo, hi = oi.encode_slabs(x)
+    assert q.shape == x.shape and lo.shape == hi.shape == (5, 3)
+    for i in range(5):
+        for h in range(3):
+            s = x[i, h]
+            assert lo[i, h] == s.min() and hi[i, h] == s.max()
+            assert q[i, h].flat[np.argmin(s)] == 0 and q[i, h].flat[np.argmax(s)] == 255
+            step = (float(hi[i, h]) - float(lo[i, h])) / 255.0
+            assert np.abs(oi.decode_f64(q[i, h], lo[i, h], hi[i, h]) - s).max() <= 0.5 * step * (1 + 1e-5)
+
+
+def test_pool_quantisation_of_mixed_row_counts():
+    # blocks with different used-row counts: every (block, head) slab has the
+    # range of its used rows only, and rows past them stay zero
+    rng = np.random.default_rng(12)
+    pool = rng.normal(size=(9, 2, 16, 8)).astype(np.float32)
+    rows = [16, 1, 7, 16, 0, 7, 3, 16, 1]
+    codes, params = oi.quantize_pool(pool, rows_used=rows)
+    for b, n in enumerate(rows):
+        for h in range(2):
+            if n == 0:
+                assert (codes[b, h] == 0).all() and (params[b, h] == 0).all()
+                continue
+            s = pool[b, h, :n]
+            assert params[b, h, 0] == s.min() and params[b, h, 1] == s.max()
+            assert (codes[b, h, n:] == 0).all()
+            step = (float(s.max()) - float(s.min())) / 255.0
+            dec = oi.decode_f64(codes[b, h, :n], *params[b, h])
+            assert np.abs(dec - s).max() <= 0.5 * step * (1 + 1e-5) or step == 0
