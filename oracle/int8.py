@@ -81,8 +81,8 @@ def quantize_pool(pool_f32: np.ndarray, rows_used=None):
         if n == 0:
             continue
         blks = np.nonzero(used == n)[0]
-        for s in range(0, blks.size, 4096):    # bounded temporaries
-            part = blks[s:s + 4096]
+        for s in range(0, blks.size, 1024):    # bounded temporaries
+            part = blks[s:s + 1024]
             q, lo, hi = encode_slabs(pool_f32[part, :, :n])
             codes[part, :, :n] = q
             params[part, :, 0] = lo

@@ -6,6 +6,9 @@ the expectations come only from ``oracle``.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -97,6 +100,25 @@ class GpuCase:
                                            stream=stream)
         return self.out
 
+    def fused_step(self, partition_tokens=None, stream=None):
+        """The call the benchmark times: pkv_paged_decode_step[_fp8] (slot
+        mapping, append and attention in the decode launch, then the combine)."""
+        import paged_kv_cache_153_gb300 as pkv
+        w = self.w
+        pt = w.partition_tokens if partition_tokens is None else partition_tokens
+        ws = self.workspace(pt)
+        if self.fp8:
+            pkv.pkv_paged_decode_step_fp8(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache, self.k_scale,
+                                          self.v_scale, self.tables, self.lens, self.out, scale=w.scale,
+                                          max_context_len=self.max_ctx, workspace=ws, partition_tokens=pt,
+                                          slot_mapping_out=self.slots, err_flag=self.err, stream=stream)
+        else:
+            pkv.pkv_paged_decode_step(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache, self.tables,
+                                      self.lens, self.out, scale=w.scale, max_context_len=self.max_ctx,
+                                      workspace=ws, partition_tokens=pt, slot_mapping_out=self.slots,
+                                      err_flag=self.err, stream=stream)
+        return self.out
+
     def err_code(self) -> int:
         torch.cuda.synchronize()
         return int(self.err.item())
@@ -136,6 +158,68 @@ def oracle_fp8_codes(w: wl.Workload):
         kn[:, g] = oe.encode(wl.bits_to_f32(w.k_new[:, g], w.dtype), w.k_scale[g])
         vn[:, g] = oe.encode(wl.bits_to_f32(w.v_new[:, g], w.dtype), w.v_scale[g])
     return kc, vc, kn, vn
+
+
+def fp8_codes_by_table(bits: np.ndarray, dtype: str, scale) -> np.ndarray:
+    """The oracle's E4M3 codes of 16-bit data ``bits`` with one scale: the
+    oracle's encoder is applied to every one of the 65,536 bit patterns once
+    and the data are looked up in that table (the code of a value depends only
+    on its bits and the scale)."""
+    table = oe.encode(wl.bits_to_f32(np.arange(1 << 16, dtype=np.uint16), dtype), scale)
+    return table[np.asarray(bits, dtype=np.uint16)]
+
+
+def oracle_fp8_pool_codes(w: wl.Workload, pool: np.ndarray, scales) -> np.ndarray:
+    """Oracle E4M3 codes of a whole pool [NB, H, 16, d] (or rows [T, H, d]),
+    per KV head with that head's scale, through the per-head code table."""
+    out = np.empty(pool.shape, dtype=np.uint8)
+    for g in range(w.n_kv_heads):
+        out[:, g] = fp8_codes_by_table(pool[:, g], w.dtype, scales[g])
+    return out
+
+
+def oracle_decode_all(w: wl.Workload, kp, vp, seqs=None):
+    """float64 expectation [B, Hq, d] (rows of sequences not in ``seqs`` are
+    NaN), gathering each (sequence, KV head) once."""
+    q = on.bits_to_f64(w.q, w.dtype)
+    group = w.n_q_heads // w.n_kv_heads
+    ref = np.full((w.batch, w.n_q_heads, w.head_dim), np.nan)
+    for b in (range(w.batch) if seqs is None else seqs):
+        n = int(w.context_lens[b])
+        for g in range(w.n_kv_heads):
+            kb = oa.gather_sequence(kp, w.block_tables[b], n, g)
+            vb = oa.gather_sequence(vp, w.block_tables[b], n, g)
+            if w.kv_dtype == "e4m3":
+                keys = oe.decode(kb) * float(w.k_scale[g])
+                values = oe.decode(vb) * float(w.v_scale[g])
+            else:
+                keys = on.bits_to_f64(kb, w.kv_dtype)
+                values = on.bits_to_f64(vb, w.kv_dtype)
+            for h in range(g * group, (g + 1) * group):
+                ref[b, h] = oa.attend(q[b, h], keys, values, w.scale)
+    return ref
+
+
+def compare_all(got: torch.Tensor, ref: np.ndarray, atol: float, rtol: float):
+    """Elementwise |got - ref| <= atol + rtol |ref| over the rows of ``ref``
+    that are not NaN; returns (max_abs, max_rel, n_bad, n_checked)."""
+    g = got.float().cpu().numpy().astype(np.float64)
+    sel = ~np.isnan(ref)
+    diff = np.abs(g[sel] - ref[sel])
+    lim = atol + rtol * np.abs(ref[sel])
+    rel = diff / np.maximum(np.abs(ref[sel]), 1e-30)
+    return float(diff.max()), float(rel.max()), int((diff > lim).sum()) + int(np.isnan(g[sel]).sum()), int(sel.sum())
+
+
+def record_parity(label: str, **fields) -> None:
+    """Print a parity record and append it, as one JSON line, to the file
+    named by PKV_PARITY_LOG (if set)."""
+    rec = {"case": label, **fields}
+    print("parity", json.dumps(rec))
+    path = os.environ.get("PKV_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
 
 
 def oracle_decode(w: wl.Workload, kp, vp, pairs=None):
