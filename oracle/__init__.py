@@ -33,6 +33,7 @@ block_pool   the physical block pool, refcounts and per-sequence block tables.
 slots        slot mapping: logical position -> physical slot.
 append       writing new K/V rows into their slots (a bit copy).
 e4m3         the OCP FP8 E4M3 code table, encoder and decoder.
+e5m2         the OCP FP8 E5M2 code table, encoder and decoder.
 int8         INT8 codes with per-block min-max scaling (encode, decode, re-quantising append).
 attention    paged decode attention and the contiguous (no-cache) comparator.
 prefill      paged prefill / extend attention (causal over the cached context).

@@ -45,9 +45,10 @@ Conventions of every workload:
     end, holds N(0, 1) data, so a kernel that reads past the end is caught.
   * 16-bit data is stored as uint16 bit patterns (fp16 or bf16, rounded to
     nearest-even from float32 draws).
-  * For the E4M3 workload the pool and new rows hold the bf16 data before
-    quantisation and ``k_scale``/``v_scale`` are per-KV-head calibration scales:
-    absmax over that head's data divided by 448 (the E4M3 maximum), i.e. the
+  * For an FP8 cache ("e4m3" or "e5m2") the pool and new rows hold the 16-bit
+    data before quantisation and ``k_scale``/``v_scale`` are per-KV-head
+    calibration scales: absmax over that head's data divided by the format's
+    largest finite value (448 for E4M3, 57344 for E5M2), i.e. the
     absmax-calibrated per-head scale the FP8 roll-out advice asks for; they are
     inputs of the method, not part of it.
 """
@@ -61,6 +62,9 @@ import numpy as np
 BLOCK_SIZE = 16
 
 CONFIG_NAMES = ("tiny", "mha7b", "gqa8b", "prefix", "fp8long")
+
+# largest finite value of each FP8 storage format (the calibration divisor)
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
 CONFIG_SEEDS = {name: 1000 + i for i, name in enumerate(CONFIG_NAMES)}
 
 
@@ -72,17 +76,17 @@ class Workload:
     n_kv_heads: int
     head_dim: int
     dtype: str                  # q / out / new-row dtype: "f16" | "bf16"
-    kv_dtype: str               # cache dtype: "f16" | "bf16" | "e4m3"
+    kv_dtype: str               # cache dtype: "f16" | "bf16" | "e4m3" | "e5m2"
     scale: float                # softmax scale 1/sqrt(head_dim)
     num_blocks: int
     context_lens: np.ndarray    # int32 [B]
     block_tables: np.ndarray    # int32 [B, max_blocks_per_seq], -1 padded
     q: np.ndarray               # uint16 [B, Hq, d]
-    k_pool: np.ndarray          # uint16 [NB, Hkv, bs, d]  (pre-quantisation for e4m3)
+    k_pool: np.ndarray          # uint16 [NB, Hkv, bs, d]  (pre-quantisation for FP8)
     v_pool: np.ndarray
     k_new: np.ndarray           # uint16 [B, Hkv, d]
     v_new: np.ndarray
-    k_scale: np.ndarray | None = None   # float32 [Hkv] (e4m3 only)
+    k_scale: np.ndarray | None = None   # float32 [Hkv] (FP8 only)
     v_scale: np.ndarray | None = None
     partition_tokens: int = 0   # 0 = let the planner choose
     block_size: int = BLOCK_SIZE
@@ -93,8 +97,12 @@ class Workload:
         return int(self.block_tables.shape[1])
 
     @property
+    def fp8(self) -> bool:
+        return self.kv_dtype in FP8_MAX
+
+    @property
     def kv_elt_bytes(self) -> int:
-        return 1 if self.kv_dtype == "e4m3" else 2
+        return 1 if self.fp8 else 2
 
     @property
     def q_elt_bytes(self) -> int:
@@ -207,16 +215,17 @@ def build(name: str, *, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: i
     else:
         tables = _tables_from_ids(perm, private, max_blocks)
 
-    raw_dtype = dtype if kv_dtype == "e4m3" else kv_dtype
+    raw_dtype = dtype if kv_dtype in FP8_MAX else kv_dtype
     q = _normal_bits(rng, (batch, n_q_heads, head_dim), dtype)
     k_pool = _normal_bits(rng, (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim), raw_dtype)
     v_pool = _normal_bits(rng, (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim), raw_dtype)
     k_new = _normal_bits(rng, (batch, n_kv_heads, head_dim), raw_dtype)
     v_new = _normal_bits(rng, (batch, n_kv_heads, head_dim), raw_dtype)
     k_scale = v_scale = None
-    if kv_dtype == "e4m3":
-        k_scale = (_absmax_over_head(k_pool, k_new, raw_dtype) / np.float32(448.0)).astype(np.float32)
-        v_scale = (_absmax_over_head(v_pool, v_new, raw_dtype) / np.float32(448.0)).astype(np.float32)
+    if kv_dtype in FP8_MAX:
+        top = np.float32(FP8_MAX[kv_dtype])
+        k_scale = (_absmax_over_head(k_pool, k_new, raw_dtype) / top).astype(np.float32)
+        v_scale = (_absmax_over_head(v_pool, v_new, raw_dtype) / top).astype(np.float32)
     return Workload(
         name=name, batch=batch, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads,
         head_dim=head_dim, dtype=dtype, kv_dtype=kv_dtype,
