@@ -66,7 +66,7 @@ def describe(w: wl.Workload) -> dict:
 # stays valid while these files are unchanged
 _COMMON_SOURCES = ("pkv_common.cuh", "host_util.h")
 _DECODE_SOURCES = ("api.cu", "decode.cuh", "decode_launch.cuh", "decode_f16.cu", "decode_bf16.cu",
-                   "decode_e4m3.cu", "decode_int8.cu")
+                   "decode_e4m3.cu", "decode_e5m2.cu", "decode_int8.cu")
 KERNEL_SOURCES = {
     "decode": _COMMON_SOURCES + _DECODE_SOURCES,
     "int8": _COMMON_SOURCES + _DECODE_SOURCES + ("append.cu", "append_int8.cu"),

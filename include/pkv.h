@@ -115,6 +115,22 @@ pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, const int64_t
                              int block_size, pkv_dtype in_dtype, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * E5M2 append ("KV cache capacity planning ...", section 4: the second FP8
+ * format it names, with the wider exponent range and the lower precision; the
+ * OCP 8-bit floating point specification of its reference list: bias 15, two
+ * mantissa bits, largest finite value 57344).  Stores
+ *     code = E5M2_RN_satfinite(fl32(x) / k_scale[h])
+ * (IEEE fp32 division, round to nearest even, magnitudes above 57344 --
+ * infinities included -- clamp to 57344, NaN stores a NaN code) for every
+ * element x of k_new (in_dtype) into the uint8 cache, and the same for V with
+ * v_scale.  Arguments, layout and errors as in pkv_kv_append_fp8.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_kv_append_e5m2(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                              int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                              const float* k_scale, const float* v_scale, int num_kv_heads, int head_dim,
+                              int block_size, pkv_dtype in_dtype, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Workspace for decode attention, in bytes, on the current CUDA device.  The
  * decode splits the work over the flattened (sequence, KV head, block) space;
  * pieces of a sequence handled by different thread blocks leave fp32 partial
@@ -210,6 +226,22 @@ pkv_status pkv_paged_decode_attention_fp8(const void* q, const uint8_t* k_cache,
                                           void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged decode attention over an E5M2 cache (uint8 codes, as stored by
+ * pkv_kv_append_e5m2) with per-KV-head scales: K_j and V_j are
+ * E5M2(code) * k_scale[g] and E5M2(code) * v_scale[g], dequantised in
+ * registers before the arithmetic ("KV cache capacity planning ...", sections
+ * 4 and 5).  Arguments as in pkv_paged_decode_attention_fp8.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_attention_e5m2(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                           const float* k_scale, const float* v_scale,
+                                           const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                           int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                           float scale, void* out, pkv_dtype q_dtype, int partition_tokens,
+                                           void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                           void* stream);
+
+/* ---------------------------------------------------------------------------
  * One whole decode step in a single decode launch (plus the partial merge):
  * for every sequence b, append k_new[b] / v_new[b] at position
  * p = context_lens[b] - 1 (slot = block_tables[b][p / 16] * 16 + p % 16,
@@ -242,6 +274,19 @@ pkv_status pkv_paged_decode_step_fp8(const void* q, const void* k_new, const voi
                                      int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale,
                                      void* out, pkv_dtype q_dtype, int partition_tokens, int64_t* slot_mapping_out,
                                      void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The same fused step over an E5M2 cache: the new rows (q_dtype) are stored as
+ * pkv_kv_append_e5m2 stores them, and attention uses those codes, as
+ * pkv_paged_decode_attention_e5m2.  Arguments as in pkv_paged_decode_step_fp8.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_step_e5m2(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
+                                      uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                                      const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int64_t num_blocks, int max_context_len, float scale,
+                                      void* out, pkv_dtype q_dtype, int partition_tokens, int64_t* slot_mapping_out,
+                                      void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
  * One whole decode step from HOST buffers: copies q, k_new, v_new,

@@ -24,6 +24,7 @@ __all__ = [
     "BlockPool", "pkv_blocks_needed", "pkv_version", "pkv_status_string", "pkv_last_error",
     "pkv_copy_blocks", "pkv_prepare_append", "pkv_paged_prefill_attention", "pkv_paged_decode_step_layer",
     "StepGraph", "pkv_kv_quantize_int8", "pkv_kv_append_int8", "pkv_paged_decode_attention_int8",
+    "pkv_kv_append_e5m2", "pkv_paged_decode_attention_e5m2", "pkv_paged_decode_step_e5m2",
 ]
 
 PKV_F16 = 0
@@ -62,15 +63,20 @@ _SIGS = {
     "pkv_slot_mapping": (_i, [_p, _i, _i64, _p, _p, C.c_int32, _i64, _i, _p, _p, _p]),
     "pkv_kv_append": (_i, [_p, _p, _p, _i64, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
     "pkv_kv_append_fp8": (_i, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i, _i, _i, _i, _p, _p]),
+    "pkv_kv_append_e5m2": (_i, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i, _i, _i, _i, _p, _p]),
     "pkv_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "pkv_paged_decode_attention": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i, _i,
                                         _p, _sz, _p, _p]),
     "pkv_paged_decode_attention_fp8": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f,
                                             _p, _i, _i, _p, _sz, _p, _p]),
+    "pkv_paged_decode_attention_e5m2": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f,
+                                             _p, _i, _i, _p, _sz, _p, _p]),
     "pkv_paged_decode_step": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i, _i, _p,
                                    _p, _sz, _p, _p]),
     "pkv_paged_decode_step_fp8": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p,
                                        _i, _i, _p, _p, _sz, _p, _p]),
+    "pkv_paged_decode_step_e5m2": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f,
+                                        _p, _i, _i, _p, _p, _sz, _p, _p]),
     "pkv_paged_decode_attention_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
                                                 _i, _p, _p]),
     "pkv_decode_step_host": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i,
@@ -170,13 +176,26 @@ def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, *, dtype=None, e
         nb, hkv, d, bs, _dtype_code(k_new, dtype), _ptr(err_flag), _stream(stream)))
 
 
-def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, *, in_dtype=None,
-                      err_flag=None, stream=None) -> None:
+def _append_fp8(fn, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, in_dtype, err_flag, stream):
     nb, hkv, bs, d = k_cache.shape
-    _check("pkv_kv_append_fp8", lib.pkv_kv_append_fp8(
+    _check(fn, getattr(lib, fn)(
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), slot_mapping.numel(), _ptr(k_cache), _ptr(v_cache),
         nb, _ptr(k_scale), _ptr(v_scale), hkv, d, bs, _dtype_code(k_new, in_dtype), _ptr(err_flag),
         _stream(stream)))
+
+
+def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, *, in_dtype=None,
+                      err_flag=None, stream=None) -> None:
+    """E4M3 append: uint8 caches [NB, Hkv, 16, D], fp32 per-head scales."""
+    _append_fp8("pkv_kv_append_fp8", k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, in_dtype,
+                err_flag, stream)
+
+
+def pkv_kv_append_e5m2(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, *, in_dtype=None,
+                       err_flag=None, stream=None) -> None:
+    """E5M2 append: uint8 caches [NB, Hkv, 16, D], fp32 per-head scales."""
+    _append_fp8("pkv_kv_append_e5m2", k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, in_dtype,
+                err_flag, stream)
 
 
 def pkv_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -200,16 +219,29 @@ def pkv_paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, 
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
 
 
-def pkv_paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, *,
-                                   scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
-                                   q_dtype=None, err_flag=None, stream=None) -> None:
+def _decode_fp8(fn, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, scale,
+                max_context_len, workspace, partition_tokens, q_dtype, err_flag, stream):
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
-    _check("pkv_paged_decode_attention_fp8", lib.pkv_paged_decode_attention_fp8(
+    _check(fn, getattr(lib, fn)(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
         _ptr(context_lens), b, hq, hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale, _ptr(out),
         _dtype_code(q, q_dtype), partition_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, *,
+                                   scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                                   q_dtype=None, err_flag=None, stream=None) -> None:
+    _decode_fp8("pkv_paged_decode_attention_fp8", q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                context_lens, out, scale, max_context_len, workspace, partition_tokens, q_dtype, err_flag, stream)
+
+
+def pkv_paged_decode_attention_e5m2(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, *,
+                                    scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                                    q_dtype=None, err_flag=None, stream=None) -> None:
+    _decode_fp8("pkv_paged_decode_attention_e5m2", q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                context_lens, out, scale, max_context_len, workspace, partition_tokens, q_dtype, err_flag, stream)
 
 
 def pkv_paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, *, scale: float,
@@ -224,16 +256,31 @@ def pkv_paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, conte
         _ptr(err_flag), _stream(stream)))
 
 
-def pkv_paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                              out, *, scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
-                              slot_mapping_out=None, q_dtype=None, err_flag=None, stream=None) -> None:
+def _step_fp8(fn, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, scale,
+              max_context_len, workspace, partition_tokens, slot_mapping_out, q_dtype, err_flag, stream):
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
-    _check("pkv_paged_decode_step_fp8", lib.pkv_paged_decode_step_fp8(
+    _check(fn, getattr(lib, fn)(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
         _ptr(block_tables), _ptr(context_lens), b, hq, hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale,
         _ptr(out), _dtype_code(q, q_dtype), partition_tokens, _ptr(slot_mapping_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                              out, *, scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                              slot_mapping_out=None, q_dtype=None, err_flag=None, stream=None) -> None:
+    _step_fp8("pkv_paged_decode_step_fp8", q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+              context_lens, out, scale, max_context_len, workspace, partition_tokens, slot_mapping_out, q_dtype,
+              err_flag, stream)
+
+
+def pkv_paged_decode_step_e5m2(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                               out, *, scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                               slot_mapping_out=None, q_dtype=None, err_flag=None, stream=None) -> None:
+    _step_fp8("pkv_paged_decode_step_e5m2", q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+              context_lens, out, scale, max_context_len, workspace, partition_tokens, slot_mapping_out, q_dtype,
+              err_flag, stream)
 
 
 def pkv_paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, out, *, scale: float,

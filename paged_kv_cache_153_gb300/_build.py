@@ -24,8 +24,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpkv.so")
 PREFILL_LIB_PATH = os.path.join(PKG_DIR, "libpkv_prefill.so")
 
-CUDA_SOURCES = ["append.cu", "api.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "noalloc.cu",
-                "decode_int8.cu", "append_int8.cu"]
+CUDA_SOURCES = ["append.cu", "api.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "decode_e5m2.cu",
+                "noalloc.cu", "decode_int8.cu", "append_int8.cu"]
 PREFILL_SOURCES = ["prefill.cu"]
 CXX_SOURCES = ["pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -121,8 +121,8 @@ pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const 
                          int64_t* slots_out = nullptr, int num_layers = 1, int layer = 0,
                          const void* slab_params = nullptr) {
   // kv_kind: 0 = 16-bit cache, 1 = E4M3 with per-head scales, 2 = INT8 with
-  // per-(block, head) min-max parameters
-  const bool fp8 = kv_kind == 1, int8 = kv_kind == 2;
+  // per-(block, head) min-max parameters, 3 = E5M2 with per-head scales
+  const bool fp8 = kv_kind == 1 || kv_kind == 3, int8 = kv_kind == 2;
   if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks < 0 ||
       max_context_len < 0 || partition_tokens < 0 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
@@ -153,6 +153,7 @@ pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const 
   if (int8 && (!slab_params || (reinterpret_cast<uintptr_t>(slab_params) & 15u) || k_new != nullptr))
     return PKV_ERR_INVALID_ARG;
   DecodeLauncher launch = int8 ? decode_launcher_int8(dtype, head_dim, group)
+                        : kv_kind == 3 ? decode_launcher_e5m2(dtype, head_dim, group)
                         : fp8 ? decode_launcher_e4m3(dtype, head_dim, group)
                               : (dtype == PKV_F16 ? decode_launcher_f16(head_dim, group)
                                                   : decode_launcher_bf16(head_dim, group));
@@ -264,6 +265,36 @@ extern "C" pkv_status pkv_paged_decode_attention_fp8(const void* q, const uint8_
                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
                        max_context_len, scale, out, q_dtype, partition_tokens, workspace, workspace_bytes,
                        err_flag, stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_attention_e5m2(const void* q, const uint8_t* k_cache,
+                                                      const uint8_t* v_cache, const float* k_scale,
+                                                      const float* v_scale, const int32_t* block_tables,
+                                                      const int32_t* context_lens, int batch, int num_q_heads,
+                                                      int num_kv_heads, int head_dim, int block_size,
+                                                      int max_blocks_per_seq, int64_t num_blocks,
+                                                      int max_context_len, float scale, void* out,
+                                                      pkv_dtype q_dtype, int partition_tokens, void* workspace,
+                                                      size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return decode_common(3, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_context_len, scale,
+                       out, q_dtype, partition_tokens, workspace, workspace_bytes, err_flag, stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_step_e5m2(const void* q, const void* k_new, const void* v_new,
+                                                 uint8_t* k_cache, uint8_t* v_cache, const float* k_scale,
+                                                 const float* v_scale, const int32_t* block_tables,
+                                                 const int32_t* context_lens, int batch, int num_q_heads,
+                                                 int num_kv_heads, int head_dim, int block_size,
+                                                 int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                                 float scale, void* out, pkv_dtype q_dtype, int partition_tokens,
+                                                 int64_t* slot_mapping_out, void* workspace, size_t workspace_bytes,
+                                                 int32_t* err_flag, void* stream) {
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  return decode_common(3, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_context_len, scale,
+                       out, q_dtype, partition_tokens, workspace, workspace_bytes, err_flag, stream, k_new, v_new,
+                       slot_mapping_out);
 }
 
 extern "C" pkv_status pkv_paged_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,

@@ -5,8 +5,8 @@
 // "Series 03: why the KV cache eats memory, and how PagedAttention pages it",
 // section 3.1).  Append writes the token's K/V rows into that slot ("KV Cache,
 // the memory notepad of LLM inference", section 三), as a bit copy or, for the
-// E4M3 cache of "KV cache capacity planning ..." section 4, as
-// E4M3_RN_satfinite(fl32(x) / scale[h]).
+// FP8 caches of "KV cache capacity planning ..." section 4 (E4M3 or E5M2), as
+// FP8_RN_satfinite(fl32(x) / scale[h]).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -74,8 +74,9 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
     k_cache[dst] = k_new[i];
 }
 
-// One thread quantises 8 elements (16 input bytes -> 8 code bytes).
-template <typename IN>
+// One thread quantises 8 elements (16 input bytes -> 8 code bytes) to the
+// FP8 format FMT.
+template <typename FMT, typename IN>
 __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                                      const int64_t* __restrict__ slots, int64_t n_tokens,
                                      uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
@@ -98,7 +99,7 @@ __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint
     return;
   }
   const float scale = is_v ? v_scale[h] : k_scale[h];
-  const uint2 packed = quant8_e4m3(is_v ? &v_new[i] : &k_new[i], scale, IN{});
+  const uint2 packed = quant8_fp8<FMT>(is_v ? &v_new[i] : &k_new[i], scale, IN{});
   const int64_t blk = s / kBlockSize, off = s % kBlockSize;
   const int64_t dst = ((blk * n_heads + h) * kBlockSize + off) * chunks_per_row + c;
   if (is_v)
@@ -235,11 +236,14 @@ extern "C" pkv_status pkv_kv_append(const void* k_new, const void* v_new, const 
   return cuda_failed(e, "kv_append_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }
 
-extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
-                                        int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
-                                        int64_t num_blocks, const float* k_scale, const float* v_scale,
-                                        int num_kv_heads, int head_dim, int block_size, pkv_dtype in_dtype,
-                                        int32_t* err_flag, void* stream) {
+namespace pkv {
+namespace {
+
+template <typename FMT>
+pkv_status append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t num_tokens,
+                      uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks, const float* k_scale,
+                      const float* v_scale, int num_kv_heads, int head_dim, int block_size, pkv_dtype in_dtype,
+                      int32_t* err_flag, void* stream, const char* what) {
   if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
   if (in_dtype != PKV_F16 && in_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
@@ -253,12 +257,35 @@ extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, co
   const int threads = 256;
   const unsigned grid = static_cast<unsigned>((total + threads - 1) / threads);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto kern = (in_dtype == PKV_F16) ? kv_append_fp8_kernel<F16> : kv_append_fp8_kernel<BF16>;
+  auto kern = (in_dtype == PKV_F16) ? kv_append_fp8_kernel<FMT, F16> : kv_append_fp8_kernel<FMT, BF16>;
   const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(threads), 0, s, static_cast<const uint4*>(k_new),
                                    static_cast<const uint4*>(v_new), slot_mapping, num_tokens,
                                    reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale,
                                    v_scale, num_blocks * kBlockSize, num_kv_heads, chunks, err_flag);
-  return cuda_failed(e, "kv_append_fp8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
+  return cuda_failed(e, what) ? PKV_ERR_CUDA : PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                        int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                        int64_t num_blocks, const float* k_scale, const float* v_scale,
+                                        int num_kv_heads, int head_dim, int block_size, pkv_dtype in_dtype,
+                                        int32_t* err_flag, void* stream) {
+  return pkv::append_fp8<E4M3>(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, k_scale,
+                               v_scale, num_kv_heads, head_dim, block_size, in_dtype, err_flag, stream,
+                               "kv_append_fp8_kernel launch");
+}
+
+extern "C" pkv_status pkv_kv_append_e5m2(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                         int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                         int64_t num_blocks, const float* k_scale, const float* v_scale,
+                                         int num_kv_heads, int head_dim, int block_size, pkv_dtype in_dtype,
+                                         int32_t* err_flag, void* stream) {
+  return pkv::append_fp8<E5M2>(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, k_scale,
+                               v_scale, num_kv_heads, head_dim, block_size, in_dtype, err_flag, stream,
+                               "kv_append_fp8_kernel launch (E5M2)");
 }
 
 extern "C" pkv_status pkv_copy_blocks(const int32_t* src_blocks, const int32_t* dst_blocks, int64_t num_pairs,

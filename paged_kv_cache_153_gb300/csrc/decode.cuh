@@ -32,11 +32,11 @@
 //
 // Consumers.  Scores are kept in the log2 domain (scale * log2(e) applied in
 // fp32), so exponentials are exp2.
-//  * CUDA-core consumer (G = 1; E4M3 with 64-byte rows): a token row is split over
+//  * CUDA-core consumer (G = 1; FP8 with 64-byte rows): a token row is split over
 //    LPT = D / 8 lanes; partial dot products are reduced by a butterfly
 //    reduce-scatter; p is shared through a per-warp scratch row; p.V
 //    accumulates in fp32 registers, each lane owning 8 output elements.
-//  * Tensor-core consumer (G >= 2; 16-bit cache, or E4M3 with 128-byte rows
+//  * Tensor-core consumer (G >= 2; 16-bit cache, or FP8 with 128-byte rows
 //    converted to f16 in registers): q.K^T of a block is one
 //    mma.m16n8k16 per 16 head_dim elements with the 16 tokens as M and the G
 //    query heads (zero-padded to 8) as N; the fp32 scores of the C fragment
@@ -69,7 +69,7 @@ struct DecodeParams {
   const void* q;                 // [B, Hq, D] 16-bit
   const void* k_cache;           // [NB, Hkv, 16, D] KV element type
   const void* v_cache;
-  const float* k_scale;          // [Hkv] (E4M3 cache only)
+  const float* k_scale;          // [Hkv] (FP8 cache only)
   const float* v_scale;
   const float4* slab_params;     // INT8 cache: [NB * block_heads] (k_min, k_max, v_min, v_max)
   const int32_t* block_tables;   // [B, max_blocks_per_seq]
@@ -275,10 +275,11 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(w & 0xffffu)));
   return r;
 }
-// two one-byte codes (bits 0-15 of w) -> packed f16x2, exactly: E4M3 values,
-// or INT8 codes offset by 1024 (0x64cc is 1024 + cc in f16, one byte permute;
+// two one-byte codes (bits 0-15 of w) -> packed f16x2, exactly: E4M3 or E5M2
+// values (every one is a half), or INT8 codes offset by 1024 (0x64cc is 1024 + cc in f16, one byte permute;
 // the consumer folds the offset into its per-block affine terms)
 __device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, E4M3) { return e4m3x2_to_f16x2(w); }
+__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, E5M2) { return e5m2x2_to_f16x2(w); }
 __device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, U8) { return __byte_perm(w, 0x64u, 0x4140u); }
 
 
@@ -291,12 +292,12 @@ __device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int row, int chunk) 
 // ---------------------------------------------------------------------------
 // fused step: write the new token's K and V rows over row r of a staged block
 // (swizzled [16 x 128 B] sub-tiles for the tensor-core layout, linear rows
-// otherwise).  One lane per 16-byte chunk of a cache row; E4M3 rows are
-// quantised exactly as the append kernel does.
+// otherwise).  One lane per 16-byte chunk of a cache row; FP8 (E4M3 or E5M2)
+// rows are quantised exactly as the append kernel does.
 // ---------------------------------------------------------------------------
 // (out of line: it runs once per (sequence, KV head) and must not raise the
 // register allocation of the consumer loop)
-template <typename NT, int D, int ESZ, bool SWZ>
+template <typename NT, typename KV, int D, int ESZ, bool SWZ>
 __device__ __noinline__ void patch_new_row(uint32_t kslab, uint32_t vslab, int r, const void* k_row,
                                               const void* v_row, float kscale, float vscale, int lane) {
   constexpr int kChunks = D * ESZ / 16;    // 16-byte chunks per cache row
@@ -306,12 +307,12 @@ __device__ __noinline__ void patch_new_row(uint32_t kslab, uint32_t vslab, int r
     const uint32_t slab = is_v ? vslab : kslab;
     const uint32_t addr = SWZ ? swz_addr(slab, r, c) : slab + r * D * ESZ + c * 16;
     const unsigned char* src = static_cast<const unsigned char*>(is_v ? v_row : k_row);
-    uint4 v;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if constexpr (ESZ == 2) {
       v = *reinterpret_cast<const uint4*>(src + c * 16);
-    } else {
-      const uint2 lo = quant8_e4m3(src + c * 32, is_v ? vscale : kscale, NT{});
-      const uint2 hi = quant8_e4m3(src + c * 32 + 16, is_v ? vscale : kscale, NT{});
+    } else if constexpr (!std::is_same<KV, U8>::value) {   // (an INT8 cache has no fused append)
+      const uint2 lo = quant8_fp8<KV>(src + c * 32, is_v ? vscale : kscale, NT{});
+      const uint2 hi = quant8_fp8<KV>(src + c * 32 + 16, is_v ? vscale : kscale, NT{});
       v = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -486,8 +487,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
           static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache)) + (row * D + 8 * c) * T::kEsz;
       if constexpr (T::kEsz == 2)
         *reinterpret_cast<uint4*>(dst) = raw;
-      else
-        *reinterpret_cast<uint2*>(dst) = quant8_e4m3(&raw, is_v ? scales[Hkv + g] : scales[g], NT{});
+      else if constexpr (!std::is_same<KV, U8>::value)   // (an INT8 cache has no fused append)
+        *reinterpret_cast<uint2*>(dst) = quant8_fp8<KV>(&raw, is_v ? scales[Hkv + g] : scales[g], NT{});
     }
   }
 
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
     if constexpr (MMA) {
       // ------------------------- tensor-core consumer -------------------------
       // MT: operand type of the MMAs.  A 16-bit cache multiplies in its own
-      // type.  An E4M3 cache is converted to f16 in registers (every E4M3
+      // type.  An FP8 cache is converted to f16 in registers (every E4M3 or E5M2
       // value is exact in f16) and q is converted to f16 (exact in f16's
       // normal range); fp8 rows are 128 bytes, one swizzled sub-tile.
       constexpr bool kFp8 = (T::kEsz == 1);
@@ -770,7 +771,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         const uint32_t vslab = kslab + T::kSlab;
         if (ii == patch_ii && n_valid > 0) {
           const int64_t nr = (static_cast<int64_t>(d.b) * Hkv + d.g) * D * 2;
-          patch_new_row<NT, D, T::kEsz, true>(kslab, vslab, (d.n_tokens - 1) % kBlockSize,
+          patch_new_row<NT, KV, D, T::kEsz, true>(kslab, vslab, (d.n_tokens - 1) % kBlockSize,
                                               static_cast<const unsigned char*>(p.k_new) + nr,
                                               static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
                                               scales[Hkv + d.g], lane);
@@ -986,7 +987,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         const unsigned char* vslab = kslab + T::kSlab;
         if (ii == patch_ii && n_valid > 0) {
           const int64_t nr = (static_cast<int64_t>(d.b) * Hkv + d.g) * D * 2;
-          patch_new_row<NT, D, T::kEsz, false>(smem_u32(kslab), smem_u32(vslab), (d.n_tokens - 1) % kBlockSize,
+          patch_new_row<NT, KV, D, T::kEsz, false>(smem_u32(kslab), smem_u32(vslab), (d.n_tokens - 1) % kBlockSize,
                                                static_cast<const unsigned char*>(p.k_new) + nr,
                                                static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
                                                scales[Hkv + d.g], lane);

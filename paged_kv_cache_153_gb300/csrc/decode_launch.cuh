@@ -139,14 +139,15 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
 DecodeLauncher decode_launcher_f16(int head_dim, int group);
 DecodeLauncher decode_launcher_bf16(int head_dim, int group);
 DecodeLauncher decode_launcher_e4m3(int q_dtype, int head_dim, int group);
+DecodeLauncher decode_launcher_e5m2(int q_dtype, int head_dim, int group);
 DecodeLauncher decode_launcher_int8(int q_dtype, int head_dim, int group);
 
 constexpr int kCoreWarps = 8;   // consumer warps of the CUDA-core variant
 constexpr int kMmaWarps = 4;    // consumer warps of the tensor-core variant
 
 // G = 1 uses the CUDA-core consumer; G >= 2 over a 16-bit cache, or over a
-// one-byte (E4M3 or INT8) cache with 128-byte rows, uses the tensor-core consumer (the q-group
-// times a 16-token block is an MMA tile).
+// one-byte (E4M3, E5M2 or INT8) cache with 128-byte rows, uses the tensor-core
+// consumer (the q-group times a 16-token block is an MMA tile).
 template <typename QT, typename KV, int D, int G>
 DecodeLauncher pick_variant() {
   if constexpr (G >= 2 && (KV::kBytes == 2 || D * KV::kBytes == 128))

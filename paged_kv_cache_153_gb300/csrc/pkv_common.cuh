@@ -4,7 +4,8 @@
 //   bounded by the global timer: a wait that runs past kWaitLimitNs records
 //   PKV_ERR_TIMEOUT in the caller's error word and returns false, so no kernel
 //   here can spin forever.
-// * 16-bit / E4M3 -> fp32 conversions and the fp32 -> 16-bit output rounding.
+// * 16-bit / E4M3 / E5M2 -> fp32 conversions, the fp32 -> FP8 encoders and
+//   the fp32 -> 16-bit output rounding.
 #pragma once
 
 #include <cuda.h>
@@ -194,6 +195,11 @@ struct E4M3 {
   using storage = uint8_t;
   static constexpr int kBytes = 1;
 };
+// OCP E5M2: bias 15, two mantissa bits -- the upper byte of an IEEE half
+struct E5M2 {
+  using storage = uint8_t;
+  static constexpr int kBytes = 1;
+};
 // INT8 codes with per-(block, head) min-max scaling: x = min + q (max - min) / 255
 struct U8 {
   using storage = uint8_t;
@@ -212,6 +218,14 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, BF16) {
 __device__ __forceinline__ float2 unpack2_e4m3(uint16_t w) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(w));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// two packed E5M2 codes (low byte first) -> packed f16x2, exactly: each code
+// is the upper byte of the half with the same value
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t w) { return __byte_perm(w, 0u, 0x1404u); }
+__device__ __forceinline__ float2 unpack2_e5m2(uint32_t w) {
+  const uint32_t h2 = e5m2x2_to_f16x2(w);
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
@@ -235,6 +249,13 @@ __device__ __forceinline__ void load8(const void* p, float* f, E4M3) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+__device__ __forceinline__ void load8(const void* p, float* f, E5M2) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  float2 a = unpack2_e5m2(v.x & 0xffffu), b = unpack2_e5m2(v.x >> 16);
+  float2 c = unpack2_e5m2(v.y & 0xffffu), d = unpack2_e5m2(v.y >> 16);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
 // eight INT8 codes -> their integer values as floats (exact: 2^23 + q has q
 // in the low mantissa bits)
 __device__ __forceinline__ void load8(const void* p, float* f, U8) {
@@ -246,23 +267,30 @@ __device__ __forceinline__ void load8(const void* p, float* f, U8) {
   }
 }
 
-// two floats -> two E4M3 codes (lo in the low byte), round to nearest even,
-// magnitudes above 448 clamp to 448
-__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+// two floats -> two FP8 codes (lo in the low byte), round to nearest even,
+// magnitudes above the largest finite value (448 for E4M3, 57344 for E5M2)
+// clamp to it
+__device__ __forceinline__ uint32_t fp8x2_from_f32(float lo, float hi, E4M3) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+__device__ __forceinline__ uint32_t fp8x2_from_f32(float lo, float hi, E5M2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
-// 8 consecutive 16-bit elements -> 8 E4M3 codes of fl32(x) / scale (IEEE
-// division, not a reciprocal multiply), packed low byte first
-template <typename IN>
-__device__ __forceinline__ uint2 quant8_e4m3(const void* src, float scale, IN) {
+// 8 consecutive 16-bit elements -> 8 FP8 codes (format FMT) of fl32(x) /
+// scale (IEEE division, not a reciprocal multiply), packed low byte first
+template <typename FMT, typename IN>
+__device__ __forceinline__ uint2 quant8_fp8(const void* src, float scale, IN) {
   float x[8];
   load8(src, x, IN{});
   uint32_t w[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) w[e] = e4m3x2_from_f32(__fdiv_rn(x[2 * e], scale), __fdiv_rn(x[2 * e + 1], scale));
+  for (int e = 0; e < 4; ++e)
+    w[e] = fp8x2_from_f32(__fdiv_rn(x[2 * e], scale), __fdiv_rn(x[2 * e + 1], scale), FMT{});
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 

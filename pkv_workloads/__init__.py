@@ -239,7 +239,9 @@ def build(name: str, *, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: i
 # ----------------------------------------------------------------------------
 # the five named workloads
 # ----------------------------------------------------------------------------
-def make(name: str, seed: int | None = None) -> Workload:
+def make(name: str, seed: int | None = None, fp8: str = "e4m3") -> Workload:
+    """The named workload; ``fp8`` picks the storage format of fp8long's cache
+    ("e4m3", the configuration's own, or "e5m2"), with the same data."""
     seed = CONFIG_SEEDS[name] if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed + 7919))   # length draws
     if name == "tiny":
@@ -262,8 +264,10 @@ def make(name: str, seed: int | None = None) -> Workload:
     if name == "fp8long":
         ctx = np.full(32, 2048, dtype=np.int32)
         ctx[rng.choice(32, size=3, replace=False)] = 65536
-        return build(name, batch=32, n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="bf16",
-                     kv_dtype="e4m3", context_lens=ctx, seed=seed, partition_tokens=512)
+        if fp8 not in FP8_MAX:
+            raise KeyError(fp8)
+        return build(name if fp8 == "e4m3" else f"{name}_{fp8}", batch=32, n_q_heads=32, n_kv_heads=8,
+                     head_dim=128, dtype="bf16", kv_dtype=fp8, context_lens=ctx, seed=seed, partition_tokens=512)
     raise KeyError(name)
 
 

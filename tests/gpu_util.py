@@ -15,11 +15,14 @@ import torch
 import pkv_workloads as wl
 from oracle import attention as oa
 from oracle import e4m3 as oe
+from oracle import e5m2 as o5
 from oracle import numerics as on
 from oracle import slots as osl
 
 ATOL, RTOL = 2e-3, 1e-2          # fp16 / bf16 attention: |gpu - ref| <= ATOL + RTOL |ref|
-FP8_ATOL = 2e-2                  # E4M3 attention: |gpu - ref| <= FP8_ATOL (same codes on both sides)
+FP8_ATOL = 2e-2                  # FP8 attention: |gpu - ref| <= FP8_ATOL (same codes on both sides)
+
+FP8_ORACLE = {"e4m3": oe, "e5m2": o5}   # the oracle module of each FP8 storage format
 
 TORCH_16 = {"f16": torch.float16, "bf16": torch.bfloat16}
 
@@ -43,7 +46,8 @@ class GpuCase:
     def __init__(self, w: wl.Workload, *, codes=None, max_context_len=None):
         d = dev()
         self.w = w
-        self.fp8 = w.kv_dtype == "e4m3"
+        self.fp8 = w.fp8
+        self.fmt = w.kv_dtype
         if self.fp8:
             kc, vc = codes
             self.k_cache = torch.from_numpy(kc).to(d)
@@ -83,16 +87,17 @@ class GpuCase:
             pkv.pkv_slot_mapping(self.tables, self.lens, self.slots, num_blocks=w.num_blocks,
                                  position_offset=-1, err_flag=self.err, stream=stream)
             if self.fp8:
-                pkv.pkv_kv_append_fp8(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
-                                      self.k_scale, self.v_scale, err_flag=self.err, stream=stream)
+                append = pkv.pkv_kv_append_fp8 if self.fmt == "e4m3" else pkv.pkv_kv_append_e5m2
+                append(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                       err_flag=self.err, stream=stream)
             else:
                 pkv.pkv_kv_append(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
                                   err_flag=self.err, stream=stream)
         if self.fp8:
-            pkv.pkv_paged_decode_attention_fp8(self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
-                                               self.tables, self.lens, self.out, scale=w.scale,
-                                               max_context_len=self.max_ctx, workspace=ws,
-                                               partition_tokens=pt, err_flag=self.err, stream=stream)
+            attend = pkv.pkv_paged_decode_attention_fp8 if self.fmt == "e4m3" else pkv.pkv_paged_decode_attention_e5m2
+            attend(self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.tables, self.lens, self.out,
+                   scale=w.scale, max_context_len=self.max_ctx, workspace=ws, partition_tokens=pt,
+                   err_flag=self.err, stream=stream)
         else:
             pkv.pkv_paged_decode_attention(self.q, self.k_cache, self.v_cache, self.tables, self.lens,
                                            self.out, scale=w.scale, max_context_len=self.max_ctx,
@@ -108,10 +113,10 @@ class GpuCase:
         pt = w.partition_tokens if partition_tokens is None else partition_tokens
         ws = self.workspace(pt)
         if self.fp8:
-            pkv.pkv_paged_decode_step_fp8(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache, self.k_scale,
-                                          self.v_scale, self.tables, self.lens, self.out, scale=w.scale,
-                                          max_context_len=self.max_ctx, workspace=ws, partition_tokens=pt,
-                                          slot_mapping_out=self.slots, err_flag=self.err, stream=stream)
+            fused = pkv.pkv_paged_decode_step_fp8 if self.fmt == "e4m3" else pkv.pkv_paged_decode_step_e5m2
+            fused(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.tables,
+                  self.lens, self.out, scale=w.scale, max_context_len=self.max_ctx, workspace=ws, partition_tokens=pt,
+                  slot_mapping_out=self.slots, err_flag=self.err, stream=stream)
         else:
             pkv.pkv_paged_decode_step(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache, self.tables,
                                       self.lens, self.out, scale=w.scale, max_context_len=self.max_ctx,
@@ -134,7 +139,7 @@ def oracle_slots(w: wl.Workload) -> np.ndarray:
 def oracle_pools_after_append(w: wl.Workload):
     """Bit patterns (16-bit) or E4M3 codes of the pools after the step's append."""
     slots = oracle_slots(w)
-    if w.kv_dtype == "e4m3":
+    if w.fp8:
         kc, vc, kn, vn = oracle_fp8_codes(w)
         osl.append_rows(kc, kn, slots)
         osl.append_rows(vc, vn, slots)
@@ -146,35 +151,38 @@ def oracle_pools_after_append(w: wl.Workload):
 
 
 def oracle_fp8_codes(w: wl.Workload):
-    """Oracle E4M3 codes of the whole pool (before the append) and of the new
-    rows, per KV head with that head's scale."""
+    """Oracle FP8 codes (the workload's format) of the whole pool (before the
+    append) and of the new rows, per KV head with that head's scale."""
+    enc = FP8_ORACLE[w.kv_dtype].encode
     kc = np.empty(w.k_pool.shape, dtype=np.uint8)
     vc = np.empty(w.v_pool.shape, dtype=np.uint8)
     kn = np.empty(w.k_new.shape, dtype=np.uint8)
     vn = np.empty(w.v_new.shape, dtype=np.uint8)
     for g in range(w.n_kv_heads):
-        kc[:, g] = oe.encode(wl.bits_to_f32(w.k_pool[:, g], w.dtype), w.k_scale[g])
-        vc[:, g] = oe.encode(wl.bits_to_f32(w.v_pool[:, g], w.dtype), w.v_scale[g])
-        kn[:, g] = oe.encode(wl.bits_to_f32(w.k_new[:, g], w.dtype), w.k_scale[g])
-        vn[:, g] = oe.encode(wl.bits_to_f32(w.v_new[:, g], w.dtype), w.v_scale[g])
+        kc[:, g] = enc(wl.bits_to_f32(w.k_pool[:, g], w.dtype), w.k_scale[g])
+        vc[:, g] = enc(wl.bits_to_f32(w.v_pool[:, g], w.dtype), w.v_scale[g])
+        kn[:, g] = enc(wl.bits_to_f32(w.k_new[:, g], w.dtype), w.k_scale[g])
+        vn[:, g] = enc(wl.bits_to_f32(w.v_new[:, g], w.dtype), w.v_scale[g])
     return kc, vc, kn, vn
 
 
-def fp8_codes_by_table(bits: np.ndarray, dtype: str, scale) -> np.ndarray:
-    """The oracle's E4M3 codes of 16-bit data ``bits`` with one scale: the
-    oracle's encoder is applied to every one of the 65,536 bit patterns once
-    and the data are looked up in that table (the code of a value depends only
-    on its bits and the scale)."""
-    table = oe.encode(wl.bits_to_f32(np.arange(1 << 16, dtype=np.uint16), dtype), scale)
+def fp8_codes_by_table(bits: np.ndarray, dtype: str, scale, fmt: str = "e4m3") -> np.ndarray:
+    """The oracle's FP8 codes (format ``fmt``) of 16-bit data ``bits`` with one
+    scale: the oracle's encoder is applied to every one of the 65,536 bit
+    patterns once and the data are looked up in that table (the code of a
+    value depends only on its bits and the scale)."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        table = FP8_ORACLE[fmt].encode(wl.bits_to_f32(np.arange(1 << 16, dtype=np.uint16), dtype), scale)
     return table[np.asarray(bits, dtype=np.uint16)]
 
 
 def oracle_fp8_pool_codes(w: wl.Workload, pool: np.ndarray, scales) -> np.ndarray:
-    """Oracle E4M3 codes of a whole pool [NB, H, 16, d] (or rows [T, H, d]),
-    per KV head with that head's scale, through the per-head code table."""
+    """Oracle FP8 codes (the workload's format) of a whole pool [NB, H, 16, d]
+    (or rows [T, H, d]), per KV head with that head's scale, through the
+    per-head code table."""
     out = np.empty(pool.shape, dtype=np.uint8)
     for g in range(w.n_kv_heads):
-        out[:, g] = fp8_codes_by_table(pool[:, g], w.dtype, scales[g])
+        out[:, g] = fp8_codes_by_table(pool[:, g], w.dtype, scales[g], w.kv_dtype)
     return out
 
 
@@ -189,9 +197,9 @@ def oracle_decode_all(w: wl.Workload, kp, vp, seqs=None):
         for g in range(w.n_kv_heads):
             kb = oa.gather_sequence(kp, w.block_tables[b], n, g)
             vb = oa.gather_sequence(vp, w.block_tables[b], n, g)
-            if w.kv_dtype == "e4m3":
-                keys = oe.decode(kb) * float(w.k_scale[g])
-                values = oe.decode(vb) * float(w.v_scale[g])
+            if w.fp8:
+                keys = FP8_ORACLE[w.kv_dtype].decode(kb) * float(w.k_scale[g])
+                values = FP8_ORACLE[w.kv_dtype].decode(vb) * float(w.v_scale[g])
             else:
                 keys = on.bits_to_f64(kb, w.kv_dtype)
                 values = on.bits_to_f64(vb, w.kv_dtype)
@@ -235,9 +243,9 @@ def oracle_decode(w: wl.Workload, kp, vp, pairs=None):
         n = int(w.context_lens[b])
         kb = oa.gather_sequence(kp, w.block_tables[b], n, g)
         vb = oa.gather_sequence(vp, w.block_tables[b], n, g)
-        if w.kv_dtype == "e4m3":
-            keys = oe.decode(kb) * float(w.k_scale[g])
-            values = oe.decode(vb) * float(w.v_scale[g])
+        if w.fp8:
+            keys = FP8_ORACLE[w.kv_dtype].decode(kb) * float(w.k_scale[g])
+            values = FP8_ORACLE[w.kv_dtype].decode(vb) * float(w.v_scale[g])
         else:
             keys = on.bits_to_f64(kb, w.kv_dtype)
             values = on.bits_to_f64(vb, w.kv_dtype)
