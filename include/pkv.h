@@ -137,7 +137,12 @@ pkv_status pkv_kv_append_e5m2(const void* k_new, const void* v_new, const int64_
  * results (running max, sum, unnormalised output) that a combine kernel merges
  * by log-sum-exp.  partition_tokens = 0 sizes the balanced split (one equal
  * share per resident thread block); > 0 (a multiple of block_size) sizes a
- * split into pieces of that many tokens.  Returns 0 on invalid arguments.
+ * split into fixed partitions of that many tokens of the flattened space, an
+ * equal number of consecutive partitions per resident thread block (the
+ * partitions of one sequence and KV head that one thread block holds are
+ * merged as it streams them, so each pair leaves one partial per thread block
+ * it meets).  Returns 0 on invalid arguments or when the device cannot be
+ * queried.
  * ------------------------------------------------------------------------- */
 size_t pkv_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_blocks_per_seq, int max_context_len, int partition_tokens);
@@ -185,9 +190,9 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
  * holds until the process exits.  This function allocates nothing.
  *   - Limit: a call whose pkv_decode_workspace_bytes(...) exceeds
  *     PKV_NOALLOC_SCRATCH_BYTES (16 MiB) is refused with PKV_ERR_WORKSPACE.
- *     The balanced split (partition_tokens = 0) needs about 5 MB at most on a
- *     152-SM GPU (head_dim 128, group 8) plus 4 bytes per sequence, so it
- *     fits; a fixed partition split of many long contexts may not.
+ *     Either split needs about 5 MB at most on a 152-SM GPU (head_dim 128,
+ *     group 8) plus 8 bytes per sequence, so calls of up to about a million
+ *     sequences fit.
  *   - Set-up: every call looks up the array's device address on the current
  *     device (cudaGetSymbolAddress, which allocates nothing), so the address
  *     is right after a cudaDeviceReset too.  The first call on a device also

@@ -96,12 +96,14 @@ bool ws_layout(int batch, int n_kv_heads, int group, int head_dim, int max_block
       max_context_len < 0 || partition_tokens < 0 || num_sms <= 0)
     return false;
   if (partition_tokens % kBlockSize) return false;
+  // one range per resident decode block; a partition split never has more
+  // ranges than partitions
   int64_t ranges = static_cast<int64_t>(num_sms) * kMaxCtasPerSm;
   if (partition_tokens > 0) {
     const int64_t nblk = std::min<int64_t>(max_blocks_per_seq, (max_context_len + kBlockSize - 1) / kBlockSize);
     const int64_t w_max = static_cast<int64_t>(batch) * n_kv_heads * nblk;
     const int64_t pb = partition_tokens / kBlockSize;
-    ranges = std::max<int64_t>((w_max + pb - 1) / pb, 1);
+    ranges = std::min(ranges, std::max<int64_t>((w_max + pb - 1) / pb, 1));
   }
   w->ranges_cap = ranges;
   w->slots = 2 * ranges;

@@ -8,10 +8,10 @@
 // its section 六).
 //
 // Work decomposition.  The (sequence, KV head, logical block) triples are laid
-// out flat, sequence-major; thread block c owns the flat range
-// [c * W / R, (c + 1) * W / R) (balanced mode, R = grid size) or the ranges
-// c, c + grid, ... of `part_blocks` blocks each (partition mode).  A range is
-// cut into segments at (sequence, KV head) boundaries.  A segment holding a
+// out flat, sequence-major; thread block c owns range c of R = grid size: an
+// equal share of a cost axis (balanced mode) or an equal share of the flat
+// space's fixed partitions of `part_blocks` blocks (partition mode).  A range
+// is cut into segments at (sequence, KV head) boundaries.  A segment holding a
 // whole (sequence, KV head) writes its G outputs directly; any other segment
 // writes a fp32 partial (running max m, sum l, unnormalised o) into slot 2r
 // (the range's first segment) or 2r + 1 (its last), and the combine kernel
@@ -129,9 +129,23 @@ __device__ __forceinline__ int seq_blocks(const DecodeParams& p, int ctx, int32_
   return nb;
 }
 
-// flat index of range boundary r
-__device__ __forceinline__ int64_t range_start(int64_t r, int64_t W, int64_t R, int part_blocks) {
-  return part_blocks ? min(r * part_blocks, W) : (r * W) / R;
+// Partition mode: the flat space of W blocks is cut into NP = ceil(W / P)
+// partitions of P = part_blocks blocks (the last may be shorter), and range r
+// of R owns the consecutive partitions [floor(r NP / R), floor((r + 1) NP / R)).
+// Consecutive partitions of one (sequence, KV head) that fall in one range
+// are streamed by the same thread block as one segment: the online softmax
+// merges them in registers, so a pair leaves one partial per range it meets.
+__device__ __forceinline__ int64_t part_range_start(int64_t r, int64_t W, int64_t R, int part_blocks) {
+  const int64_t np = (W + part_blocks - 1) / part_blocks;
+  return min(((r * np) / R) * part_blocks, W);
+}
+
+// the range of partition mode that holds flat block f < W (largest r with
+// part_range_start(r) <= f)
+__device__ __forceinline__ int64_t part_range_of(int64_t f, int64_t W, int64_t R, int part_blocks) {
+  const int64_t np = (W + part_blocks - 1) / part_blocks;
+  const int64_t q = f / part_blocks;
+  return min(((q + 1) * R + np - 1) / np - 1, R - 1);
 }
 
 // Balanced ranges split a cost axis, not the block axis: every block costs
@@ -440,7 +454,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       p.ws_cum[p.batch + 1 + b] = ne[b];
     }
 
-  const int64_t R = p.part_blocks ? (W + p.part_blocks - 1) / p.part_blocks : gridDim.x;
+  const int64_t R = gridDim.x;
   const int A = p.unit_cost;
   const int64_t V = seq_cost(cum, ne, p.batch, Hkv, A);   // balanced mode: total cost
 
@@ -503,14 +517,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
     }
     uint32_t k = 0, j = 0;
-    // Segments in order: the ranges of this thread block (one in balanced
-    // mode; blockIdx.x, + gridDim.x, ... in partition mode), each cut at
-    // (sequence, KV head) boundaries.
-    const int64_t r_step = p.part_blocks ? gridDim.x : R;
+    // Segments in order: the range of this thread block, cut at (sequence,
+    // KV head) boundaries.
+    const int64_t r_step = R;
     auto bounds = [&](int64_t r, int64_t& lo, int64_t& hi) {
       if (p.part_blocks) {
-        lo = range_start(r, W, R, p.part_blocks);
-        hi = range_start(r + 1, W, R, p.part_blocks);
+        lo = part_range_start(r, W, R, p.part_blocks);
+        hi = part_range_start(r + 1, W, R, p.part_blocks);
       } else {
         lo = blocks_before_cost((r * V) / R, cum, ne, p.batch, Hkv, A);
         hi = blocks_before_cost(((r + 1) * V) / R, cum, ne, p.batch, Hkv, A);
@@ -1221,7 +1234,7 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
   const int Hkv = p.n_kv_heads;
   const int64_t W = static_cast<int64_t>(Hkv) * p.ws_cum[p.batch];
   const int64_t S0 = static_cast<int64_t>(Hkv) * c0 + static_cast<int64_t>(g) * nb;
-  const int64_t R = p.part_blocks ? (W + p.part_blocks - 1) / p.part_blocks : grid_ranges;
+  const int64_t R = grid_ranges;
   // Balanced mode works on the cost axis (see blocks_before_cost): u0 is the
   // cost where (b, g) starts, pos0 that of its first block; the block before
   // S0, if any, is the last of the previous non-empty pair, at u0 - kBlockCost.
@@ -1236,9 +1249,9 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
   int64_t r0, r1;
   bool first_is_head;
   if (p.part_blocks) {
-    r0 = S0 / p.part_blocks;
-    r1 = (S0 + nb - 1) / p.part_blocks;
-    first_is_head = (S0 == range_start(r0, W, R, p.part_blocks));
+    r0 = part_range_of(S0, W, R, p.part_blocks);
+    r1 = part_range_of(S0 + nb - 1, W, R, p.part_blocks);
+    first_is_head = (S0 == part_range_start(r0, W, R, p.part_blocks));
   } else {
     r0 = ((pos0 + 1) * R + V - 1) / V - 1;   // largest r with vr(r) <= pos0
     const int64_t posl = pos0 + static_cast<int64_t>(kBlockCost) * (nb - 1);
@@ -1248,7 +1261,7 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
   if (r0 == r1) return;   // one segment: written by the decode kernel
   // a range after r0 holds a block of (b, g) unless it is narrower than a block
   auto has_piece = [&](int64_t r) -> bool {
-    if (p.part_blocks) return range_start(r + 1, W, R, p.part_blocks) > range_start(r, W, R, p.part_blocks);
+    if (p.part_blocks) return part_range_start(r + 1, W, R, p.part_blocks) > part_range_start(r, W, R, p.part_blocks);
     if (r == r0) return true;
     const int64_t i = (vr(r) - pos0 + kBlockCost - 1) / kBlockCost;
     return pos0 + static_cast<int64_t>(kBlockCost) * i < vr(r + 1);

@@ -122,8 +122,8 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
     return PKV_ERR_CUDA;
   const int units = p.batch * p.n_kv_heads;
   if (units > 0) {
-    // fixed partitions of long contexts give many pieces per (sequence, KV
-    // head): merge those with several lanes per output
+    // a partition split of long contexts can leave many pieces per (sequence,
+    // KV head) (one per range it meets): merge those with several lanes per output
     const bool wide = p.part_blocks > 0 && (p.max_nblk + p.part_blocks - 1) / p.part_blocks >= 16;
     const cudaError_t e =
         wide ? launch_pdl(paged_decode_combine_kernel<QT, D, G, true>, dim3(units),

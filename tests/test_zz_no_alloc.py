@@ -90,15 +90,18 @@ def test_noalloc_argument_errors_match_the_workspace_entry_point(pkv):
 
 
 def test_noalloc_refuses_work_larger_than_its_scratch(pkv):
-    # a fixed 16-token partition over 64 x 8 heads of up to 65,536 tokens needs
-    # far more than the 16 MiB scratch: the call is refused before any launch
+    # the partial slots are bounded by the resident thread blocks, but the
+    # per-sequence prefixes grow with the batch: 2.5 million sequences need
+    # more than the 16 MiB scratch, and the call is refused before any launch
+    # (before q or the tables are read)
     w = wl.build("noalloc_big", batch=64, n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="bf16",
                  kv_dtype="bf16", context_lens=[16] * 64, seed=64)
     case = gu.GpuCase(w)
-    assert pkv.pkv_decode_workspace_bytes(64, 32, 8, 128, 4096, 1 << 16, 16) > 16 * 1024 * 1024
+    big = 2_500_000
+    assert pkv.pkv_decode_workspace_bytes(big, 32, 8, 128, 4096, 1 << 16, 16) > 16 * 1024 * 1024
     out = torch.empty_like(case.q)
     st = pkv.lib.pkv_paged_decode_attention_noalloc(
         case.q.data_ptr(), case.k_cache.data_ptr(), case.v_cache.data_ptr(), case.tables.data_ptr(),
-        case.lens.data_ptr(), 64, 32, 8, 128, 16, 4096, w.num_blocks, 1 << 16, C.c_float(w.scale),
+        case.lens.data_ptr(), big, 32, 8, 128, 16, 4096, w.num_blocks, 1 << 16, C.c_float(w.scale),
         out.data_ptr(), 1, 16, case.err.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == 6 and "scratch" in pkv.pkv_last_error()
