@@ -4,13 +4,21 @@ paged decode attention (split + combine), all through the libpkv C ABI.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha7b]
     python bench.py --impl reference ...      # the float64 oracle on host cores
 
-Prints one JSON line (rank 0).  The default workload is the Llama-2-7B-shaped
+Prints one JSON line (rank 0).  The headline workload is the Llama-2-7B-shaped
 MHA decode: batch 16, 32 query = 32 KV heads, head_dim 128, fp16, block 16,
 every context 4096 tokens, block tables drawn as a random permutation of a
 4096-block pool.  Its KV cache (1.07 GB read per step) is larger than L2, so
-no flush is needed between steps.  Under torchrun every rank runs its own
-replica of the workload (no data-path collective); the timing is the maximum
-over ranks and ``value`` is the tokens of all ranks divided by it.
+no flush is needed between steps.  A default run (no --workload) also times
+the other large decode configurations in the same process -- the
+Llama-3-8B-shaped GQA decode, the shared-prefix batch and the long-context
+E4M3 mix -- and reports each under "configs" with its own roofline and CPU
+baseline.  Under torchrun every rank runs its own replica of the headline
+workload (no data-path collective); the timing is the maximum over ranks and
+``value`` is the tokens of all ranks divided by it.
+
+The CPU baseline is the float64 oracle on a bounded sample of each workload,
+timed on every host core (a process pool forked before any CUDA call, one
+sequence per task) and on one core.
 """
 from __future__ import annotations
 
@@ -192,12 +200,13 @@ def oracle_step(w: wl.Workload, seqs) -> int:
     """One decode step of the float64 oracle for sequences ``seqs``: slot
     mapping, append, attention for all their query heads.  Returns tokens."""
     from oracle import attention as oa
-    from oracle import e4m3 as oe
+    from oracle import e4m3, e5m2
     from oracle import numerics as on
     from oracle import slots as osl
     seqs = list(seqs)
     slots = osl.slot_mapping(w.block_tables, seqs, w.context_lens[seqs].astype(np.int64) - 1)
-    fp8 = w.kv_dtype == "e4m3"
+    fp8 = w.fp8
+    oe = {"e4m3": e4m3, "e5m2": e5m2}.get(w.kv_dtype)
     osl.append_rows(w.k_pool, w.k_new[seqs], slots)
     osl.append_rows(w.v_pool, w.v_new[seqs], slots)
     q = on.bits_to_f64(w.q[seqs], w.dtype)
@@ -221,7 +230,36 @@ def oracle_sample_size(w: wl.Workload) -> int:
     return 2 if w.batch >= 2 else 1
 
 
-def cpu_baseline(w: wl.Workload, budget_s: float = 12.0) -> dict:
+# Host-side oracle pool.  It is forked before the first CUDA call (a process
+# forked after it can hang) and reads the workloads it was forked with.
+_POOL_WORKLOADS: dict = {}
+
+
+def _oracle_task(name_and_seq):
+    name, b = name_and_seq
+    w = _POOL_WORKLOADS[name]
+    t0 = time.perf_counter()
+    oracle_step(w, [b])
+    return time.perf_counter() - t0
+
+
+def start_oracle_pool(workloads):
+    """A fork pool of one worker per host core over ``workloads`` (call
+    before any CUDA call).  Returns (pool, cores) or (None, 1)."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    if cores < 2:
+        return None, 1
+    _POOL_WORKLOADS.clear()
+    _POOL_WORKLOADS.update({w.name: w for w in workloads})
+    return mp.get_context("fork").Pool(cores), cores
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 12.0, pool=None, cores: int = 1) -> dict:
+    """The oracle's decode step on a bounded sample of the workload: on every
+    host core through ``pool`` (sequences dealt one per task, as many rounds
+    as fit in the budget), and on one core."""
+    one_budget = budget_s if pool is None else budget_s / 3
     n = oracle_sample_size(w)
     done, t0, i = 0, time.perf_counter(), 0
     while True:
@@ -229,32 +267,61 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 12.0) -> dict:
         done += oracle_step(w, seqs)
         i += 1
         el = time.perf_counter() - t0
-        if el >= budget_s:
+        if el >= one_budget:
             break
-    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} of the workload's sequences ({n} per oracle step, all heads), float64, "
-                      f"{el:.1f} s on one host thread"}
+    one = {"value": done / el, "unit": UNIT, "cores": 1,
+           "sample": f"{done} of the workload's sequences ({n} per oracle step, all heads), float64, "
+                     f"{el:.1f} s on one host thread"}
+    if pool is None:
+        return dict(one, kind="oracle")
+    done_all, t0, rnd = 0, time.perf_counter(), 0
+    while True:
+        seqs = [(rnd * cores + j) % w.batch for j in range(cores)]
+        pool.map(_oracle_task, [(w.name, b) for b in seqs], chunksize=1)
+        done_all += len(seqs)
+        rnd += 1
+        el_all = time.perf_counter() - t0
+        if el_all >= budget_s - one_budget:
+            break
+    return {"value": done_all / el_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done_all} of the workload's sequences (all heads), float64, {el_all:.1f} s on {cores} "
+                      f"host cores (one sequence per task, {rnd} rounds)",
+            "one_core": one}
 
 
 def run_reference(args, w: wl.Workload) -> dict:
-    n = oracle_sample_size(w)
+    """The oracle as the reference arm: each step is one round of the oracle's
+    decode step over one sequence per host core (all heads), on every core."""
+    pool, cores = start_oracle_pool([w])
+    n = cores if pool is not None else oracle_sample_size(w)
+
+    def one_round(i):
+        seqs = [(i * n + j) % w.batch for j in range(n)]
+        if pool is None:
+            oracle_step(w, seqs)
+        else:
+            pool.map(_oracle_task, [(w.name, b) for b in seqs], chunksize=1)
+
     for i in range(args.warmup):
-        oracle_step(w, [(i * n + j) % w.batch for j in range(n)])
+        one_round(i)
     times = []
     for i in range(args.steps):
         t0 = time.perf_counter()
-        oracle_step(w, [(i * n + j) % w.batch for j in range(n)])
+        one_round(args.warmup + i)
         times.append(time.perf_counter() - t0)
+    if pool is not None:
+        pool.terminate()
     total = sum(times)
     value = n * args.steps / total
+    sample = (f"{n} sequences (all heads) per step of the same workload, float64 oracle, "
+              + (f"one per host core on {cores} cores" if pool is not None else "one host thread"))
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": describe(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n} sequences (all heads) per step of the same workload, float64 oracle, "
-                                   f"one host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores if pool is not None else 1, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -273,7 +340,9 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     dev = torch.device("cuda", local_rank)
     t16 = {"f16": torch.float16, "bf16": torch.bfloat16}
     stream = torch.cuda.Stream(device=dev)
-    fp8 = w.kv_dtype == "e4m3"
+    fp8 = w.fp8
+    append_fp8 = pkv.pkv_kv_append_e5m2 if w.kv_dtype == "e5m2" else pkv.pkv_kv_append_fp8
+    step_fp8 = pkv.pkv_paged_decode_step_e5m2 if w.kv_dtype == "e5m2" else pkv.pkv_paged_decode_step_fp8
     with torch.cuda.stream(stream):
         def up(bits, dt):
             return torch.from_numpy(np.ascontiguousarray(bits)).view(t16[dt]).to(dev)
@@ -295,7 +364,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
             all_slots = torch.arange(nb * bs, dtype=torch.int64, device=dev)
             kr = up(w.k_pool, w.dtype).permute(0, 2, 1, 3).reshape(nb * bs, H, D).contiguous()
             vr = up(w.v_pool, w.dtype).permute(0, 2, 1, 3).reshape(nb * bs, H, D).contiguous()
-            pkv.pkv_kv_append_fp8(kr, vr, all_slots, k_cache, v_cache, ks, vs, err_flag=err, stream=stream)
+            append_fp8(kr, vr, all_slots, k_cache, v_cache, ks, vs, err_flag=err, stream=stream)
             del kr, vr
         else:
             k_cache, v_cache = up(w.k_pool, w.kv_dtype), up(w.v_pool, w.kv_dtype)
@@ -307,10 +376,9 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
         if ev0 is not None:
             ev0.record(stream)
         if fp8:
-            pkv.pkv_paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, ks, vs, tables, lens, out,
-                                          scale=w.scale, max_context_len=max_ctx, workspace=ws,
-                                          partition_tokens=w.partition_tokens, slot_mapping_out=slots,
-                                          err_flag=err, stream=stream)
+            step_fp8(q, k_new, v_new, k_cache, v_cache, ks, vs, tables, lens, out, scale=w.scale,
+                     max_context_len=max_ctx, workspace=ws, partition_tokens=w.partition_tokens,
+                     slot_mapping_out=slots, err_flag=err, stream=stream)
         else:
             pkv.pkv_paged_decode_step(q, k_new, v_new, k_cache, v_cache, tables, lens, out, scale=w.scale,
                                       max_context_len=max_ctx, workspace=ws, partition_tokens=w.partition_tokens,
@@ -403,7 +471,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int) -> dic
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else w.kv_dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
         "config": dict(describe(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
@@ -848,6 +916,26 @@ def run_prefill(args, rank: int, local_rank: int) -> dict | None:
 
 SINGLE_GPU_WORKLOADS = ("prefill", "cow", "int8", "layers")
 
+# decode configurations a default run times after the headline one
+EXTRA_CONFIGS = ("gqa8b", "prefix", "fp8long")
+
+
+def make_workload(name: str) -> wl.Workload:
+    if name == "fp8long_e5m2":
+        return wl.make("fp8long", fp8="e5m2")
+    return wl.make(name)
+
+
+def config_summary(res: dict) -> dict:
+    """The per-configuration record of a default run: its timing, roofline,
+    clocks and end-to-end number (the headline keys of its own line)."""
+    keep = ("ms_per_step", "value", "unit", "steps", "dtype", "kv_tokens_per_s", "roofline", "clocks", "e2e",
+            "gpu_launches")
+    out = {k: res[k] for k in keep if k in res}
+    out["workload"] = res["config"]["workload"]
+    out["l2"] = res["config"]["l2"]
+    return out
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -855,10 +943,16 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha7b", choices=list(wl.CONFIG_NAMES) + ["cow", "prefill", "layers", "int8"])
+    ap.add_argument("--workload", default=None,
+                    choices=list(wl.CONFIG_NAMES) + ["fp8long_e5m2", "cow", "prefill", "layers", "int8"],
+                    help="one workload alone (default: the headline mha7b line with the other large decode "
+                         "configurations under 'configs')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    extras = args.workload is None           # the default run also times EXTRA_CONFIGS
+    if args.workload is None:
+        args.workload = "mha7b"
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -965,7 +1059,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        w = wl.make(args.workload)
+        w = make_workload(args.workload)
         print(json.dumps(run_reference(args, w)), flush=True)
         return
 
@@ -974,13 +1068,31 @@ def main():
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
-    w = wl.make(args.workload)
+    w = make_workload(args.workload)
     log(f"workload {w.name} generated")
+    others = []
+    if extras and world == 1:
+        others = [make_workload(name) for name in EXTRA_CONFIGS]
+        log("other configurations generated")
+    pool, cores = None, 1
+    if world == 1 and not args.no_cpu_baseline:
+        pool, cores = start_oracle_pool([w] + others)      # before the first CUDA call
     res = run_gpu(args, w, rank, world, local_rank)
+    if res is not None and others:
+        res["configs"] = {}
+        for ow in others:
+            sub = run_gpu(args, ow, rank, world, local_rank)
+            res["configs"][ow.name] = config_summary(sub)
     if res is not None:
-        if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(w)
+        if pool is not None:
+            res["cpu_baseline"] = cpu_baseline(w, pool=pool, cores=cores)
+            for ow in others:
+                res["configs"][ow.name]["cpu_baseline"] = cpu_baseline(ow, budget_s=6.0, pool=pool, cores=cores)
+        if extras and world == 1:
+            res["gpu_launches"] += sum(c["gpu_launches"] for c in res["configs"].values())
         print(json.dumps(res), flush=True)
+    if pool is not None:
+        pool.terminate()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
