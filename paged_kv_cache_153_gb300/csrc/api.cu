@@ -197,6 +197,13 @@ pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const 
   p.unit_cost = std::max(-1, std::min(1 << 16, env_int("PKV_UNIT_COST", -1)));
   p.slot_capacity = static_cast<int>(w.slots);
   p.qk_scale_log2 = scale * kLog2e;
+  // limit of each pipeline wait of the decode kernel: 1 s, or (for tests of
+  // the timeout path) PKV_WAIT_LIMIT_NS nanoseconds
+  {
+    const char* v = std::getenv("PKV_WAIT_LIMIT_NS");
+    const long long lim = (v != nullptr && *v != '\0') ? std::atoll(v) : 0;
+    p.wait_limit_ns = lim > 0 ? static_cast<unsigned long long>(lim) : kWaitLimitNs;
+  }
 
   LaunchInfo li{};
   li.num_sms = num_sms;

@@ -96,6 +96,7 @@ struct DecodeParams {
   int slot_capacity;             // number of partial slots in the workspace
   int stages;                    // multiple of the consumer warp count
   float qk_scale_log2;           // softmax scale * log2(e)
+  unsigned long long wait_limit_ns;   // limit of each pipeline wait (kWaitLimitNs unless overridden)
 };
 
 struct SegDesc {
@@ -213,10 +214,9 @@ struct DecodeTraits {
     return merge_off(stages) + sizeof(float) * NW * G * (D + 2);
   }
   static __host__ __device__ size_t misc_off(int stages) { return bar_off(stages) + 8 * (2 * stages + 4); }
-  // misc: stage_ok[stages], seg[2], abort (16 B), warp totals (32 ints), scales[2 * Hkv]
-  static __host__ __device__ size_t scales_off(int stages) {
-    return misc_off(stages) + 4 * stages + sizeof(SegDesc) * 2 + 16 + 4 * 32;
-  }
+  // misc: stage_ok[stages], issued[stages + 2], seg[2], abort (16 B), warp totals (32 ints), scales[2 * Hkv]
+  static __host__ __device__ size_t seg_off(int stages) { return misc_off(stages) + 4 * stages + 4 * (stages + 2); }
+  static __host__ __device__ size_t scales_off(int stages) { return seg_off(stages) + sizeof(SegDesc) * 2 + 16 + 4 * 32; }
   static __host__ __device__ size_t cum_off(int stages, int n_kv_heads) {
     return (scales_off(stages) + 4 * 2 * n_kv_heads + 15) & ~static_cast<size_t>(15);
   }
@@ -375,9 +375,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   uint64_t* qfull_bar = empty_bar + S;
   uint64_t* qempty_bar = qfull_bar + 2;
   int* stage_ok = reinterpret_cast<int*>(smem + T::misc_off(S));
-  SegDesc* seg = reinterpret_cast<SegDesc*>(smem + T::misc_off(S) + 4 * S);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc));
-  int* warp_tot = reinterpret_cast<int*>(smem + T::misc_off(S) + 4 * S + 2 * sizeof(SegDesc) + 16);
+  // issued[s]: the last use of stage s (s < S) or of query slot s - S whose
+  // phase was armed (a copy issued, or an arrival made); -1 = none
+  int* issued = stage_ok + S;
+  SegDesc* seg = reinterpret_cast<SegDesc*>(smem + T::seg_off(S));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::seg_off(S) + 2 * sizeof(SegDesc));
+  int* warp_tot = reinterpret_cast<int*>(smem + T::seg_off(S) + 2 * sizeof(SegDesc) + 16);
   float* scales = reinterpret_cast<float*>(smem + T::scales_off(S));
   int* cum = reinterpret_cast<int*>(smem + T::cum_off(S, p.n_kv_heads));   // [B + 1] block prefix
   int* ntok = cum + p.batch + 1;                                             // [B]
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 
   // ---- 1. per-sequence block counts and their prefix (all threads) -------
   if (tid == 0) *abort_flag = 0;
+  for (int x = tid; x < S + 2; x += blockDim.x) issued[x] = -1;
   for (int h = tid; h < Hkv; h += blockDim.x) {
     scales[h] = p.k_scale ? p.k_scale[h] : 1.0f;
     scales[Hkv + h] = p.v_scale ? p.v_scale[h] : 1.0f;
@@ -579,27 +583,37 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
     ProdSeg cur;
     bool have = first_from(blockIdx.x, cur);
     int ids = have ? table_at(cur, 0) : 0;
-    while (have && !*abort_flag) {
-      if (cur.slot == -2) record_error(p.err, PKV_ERR_WORKSPACE);
+    // Stopping.  A wait that runs out, or an abort raised by a consumer, stops
+    // the producer: every decision to stop is a vote of the whole warp, and
+    // after it no barrier receives another arrival (a stage or query slot
+    // whose previous copy may still be in flight is never completed by hand).
+    // Consumers stop through their own bounded waits.  Before the warp
+    // exits, lane 0 waits for the last armed phase of every stage and query
+    // slot (issued[]), so no copy is left in flight into shared memory.
+    const uint32_t full = 0xffffffffu;
+    while (have && !__any_sync(full, *abort_flag != 0)) {
+      if (cur.slot == -2 && lane == 0) record_error(p.err, PKV_ERR_WORKSPACE);
       // publish the segment descriptor and its query rows
       const int qs = j & 1;
       if (lane == 0) {
-        if (j >= 2 && !*abort_flag && !mbar_wait(&qempty_bar[qs], ((j >> 1) - 1) & 1, p.err)) *abort_flag = 1;
-        SegDesc d;
-        d.b = cur.b; d.g = cur.g; d.i0 = cur.i0; d.i1 = cur.i1; d.n_tokens = ntok[cur.b]; d.nblk = cur.nb;
-        d.slot = cur.slot;
-        d.end = *abort_flag ? 1 : 0;
-        seg[qs] = d;
-        if (!*abort_flag) {
+        const bool slot_free =
+            j < 2 || mbar_wait(&qempty_bar[qs], ((j >> 1) - 1) & 1, p.err, p.wait_limit_ns);
+        if (!slot_free || *abort_flag) {
+          *abort_flag = 1;
+        } else {
+          SegDesc d;
+          d.b = cur.b; d.g = cur.g; d.i0 = cur.i0; d.i1 = cur.i1; d.n_tokens = ntok[cur.b]; d.nblk = cur.nb;
+          d.slot = cur.slot;
+          d.end = 0;
+          seg[qs] = d;
+          issued[S + qs] = static_cast<int>(j >> 1);
           mbar_arrive_expect_tx(&qfull_bar[qs], T::kQBytes);
           bulk_g2s(q_ring + qs * T::kQBytes,
                    qbase + (static_cast<int64_t>(cur.b) * p.n_q_heads + static_cast<int64_t>(cur.g) * G) * D * 2,
                    T::kQBytes, &qfull_bar[qs], pol_stream);
-        } else {
-          mbar_arrive(&qfull_bar[qs]);
         }
       }
-      __syncwarp();
+      if (__any_sync(full, *abort_flag != 0)) break;
       ++j;
       ProdSeg nxt;
       const bool have_nxt = next_of(cur, nxt);
@@ -613,7 +627,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       const int g = cur.g;
       const int sub = S < 32 ? S : 32;
       const int nseg = cur.i1 - cur.i0;
-      for (int w0 = 0; w0 < nseg; w0 += 32) {
+      bool stop = false;
+      for (int w0 = 0; w0 < nseg && !stop; w0 += 32) {
         const int nxt_ids = (w0 + 32 < nseg) ? table_at(cur, w0 + 32) : (have_nxt ? table_at(nxt, 0) : 0);
         const int cnt = min(32, nseg - w0);
         for (int sb = 0; sb < cnt; sb += sub) {
@@ -622,39 +637,43 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             const uint32_t jw = kk / NW;                         // index in its warp's ring
             const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
             const uint32_t use = jw / SPW;
-            bool ok = ids >= 0 && ids < p.num_blocks;
-            if (use >= 1 && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.err)) {
-              *abort_flag = 1;
-              ok = false;
-            }
-            stage_ok[s] = ok ? 1 : 0;
-            unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
-            if (ok) {
-              mbar_arrive_expect_tx(&full_bar[s], T::kTx);
-              if constexpr (T::kParam > 0)
-                bulk_g2s(smem + T::prm_off(S) + s * T::kParam,
-                         p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g, T::kParam, &full_bar[s],
-                         pol_stream);
-              if constexpr (MMA) {
-                const int y = (ids * p.block_heads + g) * kBlockSize;
+            const bool stage_free = use == 0 || mbar_wait(&empty_bar[s], (use - 1) & 1, p.err, p.wait_limit_ns);
+            if (!stage_free) {
+              *abort_flag = 1;                                   // the stage is left as it is
+            } else {
+              const bool ok = ids >= 0 && ids < p.num_blocks;
+              stage_ok[s] = ok ? 1 : 0;
+              issued[s] = static_cast<int>(use);
+              unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
+              if (ok) {
+                mbar_arrive_expect_tx(&full_bar[s], T::kTx);
+                if constexpr (T::kParam > 0)
+                  bulk_g2s(smem + T::prm_off(S) + s * T::kParam,
+                           p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g, T::kParam, &full_bar[s],
+                           pol_stream);
+                if constexpr (MMA) {
+                  const int y = (ids * p.block_heads + g) * kBlockSize;
 #pragma unroll
-                for (int t = 0; t < T::kSubTiles; ++t) {
-                  tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
-                  tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
-                              pol_stream);
+                  for (int t = 0; t < T::kSubTiles; ++t) {
+                    tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
+                    tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
+                                pol_stream);
+                  }
+                } else {
+                  const int64_t slab = (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab;
+                  bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
+                  bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
                 }
               } else {
-                const int64_t slab = (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab;
-                bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
-                bulk_g2s(dst + T::kSlab, vbase + slab, T::kSlab, &full_bar[s], pol_stream);
-
+                // an id outside the pool: the stage's phase completes with no data
+                record_error(p.err, PKV_ERR_OOB);
+                mbar_arrive(&full_bar[s]);
               }
-            } else {
-              if (!*abort_flag) record_error(p.err, PKV_ERR_OOB);
-              mbar_arrive(&full_bar[s]);
             }
           }
           __syncwarp();
+          stop = __any_sync(full, *abort_flag != 0);
+          if (stop) break;
         }
         k += cnt;
         ids = nxt_ids;
@@ -662,26 +681,29 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       cur = nxt;
       have = have_nxt;
     }
-    // end marker
-    const int qs = j & 1;
+    __syncwarp();
     if (lane == 0) {
-      if (j >= 2 && !*abort_flag && !mbar_wait(&qempty_bar[qs], ((j >> 1) - 1) & 1, p.err)) *abort_flag = 1;
-      seg[qs].end = 1;
-      mbar_arrive(&qfull_bar[qs]);
-      // Before exiting, make sure no copy issued by this warp is still in
-      // flight into shared memory (one overall time limit for the drain).
-      // The last S blocks occupy S distinct stages.
-      const unsigned long long deadline = global_ns() + kWaitLimitNs;
-      const uint32_t first = k > static_cast<uint32_t>(S) ? k - S : 0;
-      for (uint32_t kk = first; kk < k; ++kk) {
-        const uint32_t jw = kk / NW;
-        const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
-        if (stage_ok[s]) mbar_wait_until(&full_bar[s], (jw / SPW) & 1, deadline);
+      // end marker (only on a normal finish)
+      const int qs = j & 1;
+      if (!*abort_flag) {
+        const bool slot_free =
+            j < 2 || mbar_wait(&qempty_bar[qs], ((j >> 1) - 1) & 1, p.err, p.wait_limit_ns);
+        if (slot_free) {
+          seg[qs].end = 1;
+          issued[S + qs] = static_cast<int>(j >> 1);
+          mbar_arrive(&qfull_bar[qs]);
+        } else {
+          *abort_flag = 1;
+        }
       }
-      // Only the last segment's query copy can still be in flight: the one
-      // before it shares its slot with the end marker, whose publication
-      // waited until the consumers had read that copy (and re-armed the slot).
-      if (j >= 1) mbar_wait_until(&qfull_bar[(j - 1) & 1], ((j - 1) >> 1) & 1, deadline);
+      // Drain: the last armed phase of each stage and query slot completes
+      // before the warp exits (earlier phases of a slot completed before it
+      // was re-armed); one overall time limit for the drain.
+      const unsigned long long deadline = global_ns() + kWaitLimitNs;
+      for (int x = 0; x < S + 2; ++x) {
+        const int u = issued[x];
+        if (u >= 0) mbar_wait_until(x < S ? &full_bar[x] : &qfull_bar[x - S], static_cast<uint32_t>(u) & 1, deadline);
+      }
     }
     __syncwarp();
     return;
@@ -702,7 +724,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   uint32_t k_base = 0;                   // CTA-local counter of the segment's first block
   while (true) {
     const int qs = j & 1;
-    const bool got = !*abort_flag && mbar_wait(&qfull_bar[qs], (j >> 1) & 1, p.err);
+    const bool got = !*abort_flag && mbar_wait(&qfull_bar[qs], (j >> 1) & 1, p.err, p.wait_limit_ns);
     if (!got) *abort_flag = 1;
     // every consumer warp must take the same exit decision (named barriers follow)
     if (named_bar_red_or(2, NW * 32, !got || seg[qs].end)) break;
@@ -774,7 +796,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         const uint32_t kk = k_base + ii;
         const uint32_t jw = kk / NW;
         const int s = warp + NW * static_cast<int>(jw % SPW);
-        if (*abort_flag || !mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err)) {
+        // (a warp vote: every lane of the warp takes the same decision)
+        const bool ready = !*abort_flag && mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, ready)) {
           *abort_flag = 1;
           break;
         }
@@ -990,7 +1014,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         const uint32_t kk = k_base + ii;
         const uint32_t jw = kk / NW;
         const int s = warp + NW * static_cast<int>(jw % SPW);
-        if (*abort_flag || !mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err)) {
+        // (a warp vote: every lane of the warp takes the same decision)
+        const bool ready = !*abort_flag && mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, ready)) {
           *abort_flag = 1;
           break;
         }
