@@ -287,3 +287,25 @@ def test_bf16_short_contexts(pkv, hq, hkv):
     case.step()
     kp, vp = gu.oracle_pools_after_append(w)
     _check(case, gu.oracle_decode(w, kp, vp), label=f"short bf16 {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("name,partition", [("gqa8b", 0), ("fp8long", 512), ("mha7b", 0)])
+def test_workspace_contents_do_not_change_the_result(pkv, name, partition):
+    # the workspace needs no initialisation: whatever an earlier call or a
+    # fill left in it, every call gives the same bits
+    w = wl.make(name)
+    if w.fp8:
+        case = gu.GpuCase(w, codes=(gu.oracle_fp8_pool_codes(w, w.k_pool, w.k_scale),
+                                    gu.oracle_fp8_pool_codes(w, w.v_pool, w.v_scale)))
+    else:
+        case = gu.GpuCase(w)
+    ws = case.workspace(partition)
+    outs = []
+    for fill in (0xFF, None, None, 0x00, None):
+        if fill is not None:
+            ws.fill_(fill)
+        case.step(partition_tokens=partition, append=False)
+        outs.append(case.out.clone())
+    torch.cuda.synchronize()
+    assert case.err_code() == 0
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
