@@ -78,9 +78,9 @@ struct DecodeParams {
   const void* k_new;             // fused step: [B, Hkv, D] rows appended at position ctx - 1 (else null)
   const void* v_new;
   int64_t* slots_out;            // fused step: [B] slots of the appended rows (nullable)
-  int32_t* ws_cum;               // [2 (B + 1)]: block-count prefix, then non-empty-sequence prefix (for the combine)
   float* ws_ml;                  // [slots, G, 2]
   float* ws_o;                   // [slots, G, D]
+  int32_t* ws_cum;               // [2 (B + 1)]: block-count prefix, then non-empty-sequence prefix (for the combine)
   int32_t* err;
   int64_t num_blocks;
   int batch;
@@ -159,6 +159,10 @@ __device__ __forceinline__ int64_t part_range_of(int64_t f, int64_t W, int64_t R
 // (cum: block prefix, ne: non-empty-sequence prefix, A = unit_cost), and
 // range r of R owns the blocks with floor(r V / R) <= pos < floor((r+1) V / R).
 constexpr int kBlockCost = 4;
+
+// batches up to this size: the combine kernel sums the block counts itself
+// (each of its thread blocks reads every context length once)
+constexpr int kCombineLocalPrefix = 256;
 
 __device__ __forceinline__ int64_t seq_cost(const int* cum, const int* ne, int b, int Hkv, int A) {
   return static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * cum[b] + static_cast<int64_t>(A) * ne[b]);
@@ -1240,14 +1244,59 @@ template <typename QT, int D, int G, bool WIDE>
 __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
     paged_decode_combine_kernel(const __grid_constant__ DecodeParams p, int grid_ranges) {
   constexpr int kSplit = combine_split<D, G, WIDE>();
-  pdl_wait_and_release();
   const int u = blockIdx.x;
   const int b = u / p.n_kv_heads, g = u % p.n_kv_heads;
   const int t = threadIdx.x / kSplit, sub = threadIdx.x % kSplit;
   const bool live_t = t < G * D / 4;
   auto* out = static_cast<typename QT::storage*>(p.out);
-  const int c0 = p.ws_cum[b], c1 = p.ws_cum[b + 1];
-  const int nb = c1 - c0;
+  // Geometry: blocks and non-empty sequences before b and in all, and the
+  // blocks of b.  For a small batch and the narrow form (small thread blocks,
+  // which become resident beside the decode grid) they are summed here from
+  // the context lengths -- an input the decode kernel does not write -- while
+  // the decode grid still runs (this launch overlaps it), clamped exactly as
+  // the decode kernel clamps them; only the partials are then read after the
+  // wait.  Otherwise the prefixes the decode kernel leaves in the workspace
+  // are read after the wait.
+  int64_t c0, ne_b, tot, tot_ne;
+  int nb;
+  if (!WIDE && p.batch <= kCombineLocalPrefix) {
+    __shared__ long long red[5][32];      // per-warp sums (up to 32 warps)
+    long long v[5] = {0, 0, 0, 0, 0};
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
+      const int ctx = p.context_lens[i];
+      const int n = ctx < 0 ? 0 : min((ctx + kBlockSize - 1) / kBlockSize, min(p.max_blocks_per_seq, p.max_nblk));
+      v[2] += n;
+      v[3] += n > 0;
+      if (i < b) {
+        v[0] += n;
+        v[1] += n > 0;
+      }
+      if (i == b) v[4] = n;
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+      if (lane == 0) red[k][wid] = v[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      v[k] = 0;
+      for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) v[k] += red[k][w2];
+    }
+    c0 = v[0], ne_b = v[1], tot = v[2], tot_ne = v[3];
+    nb = static_cast<int>(v[4]);
+    pdl_wait_and_release();
+  } else {
+    pdl_wait_and_release();
+    c0 = p.ws_cum[b];
+    nb = p.ws_cum[b + 1] - p.ws_cum[b];
+    tot = p.ws_cum[p.batch];
+    ne_b = p.ws_cum[p.batch + 1 + b];
+    tot_ne = p.ws_cum[2 * p.batch + 1];
+  }
   const int64_t base_out = (static_cast<int64_t>(b) * p.n_q_heads + g * G) * D + 4 * t;
   auto store4 = [&](float a, float b2, float c, float d) {
     const uint32_t lo = pack2(a, b2, QT{}), hi = pack2(c, d, QT{});
@@ -1258,17 +1307,17 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
     return;
   }
   const int Hkv = p.n_kv_heads;
-  const int64_t W = static_cast<int64_t>(Hkv) * p.ws_cum[p.batch];
+  const int64_t W = static_cast<int64_t>(Hkv) * tot;
   const int64_t S0 = static_cast<int64_t>(Hkv) * c0 + static_cast<int64_t>(g) * nb;
   const int64_t R = grid_ranges;
   // Balanced mode works on the cost axis (see blocks_before_cost): u0 is the
   // cost where (b, g) starts, pos0 that of its first block; the block before
   // S0, if any, is the last of the previous non-empty pair, at u0 - kBlockCost.
   const int A = p.unit_cost;
-  const int64_t V = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * p.ws_cum[p.batch] +
-                                                 static_cast<int64_t>(A) * p.ws_cum[2 * p.batch + 1]);
+  const int64_t V = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * tot +
+                                                 static_cast<int64_t>(A) * tot_ne);
   const int64_t u0 = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * c0 +
-                                                  static_cast<int64_t>(A) * p.ws_cum[p.batch + 1 + b]) +
+                                                  static_cast<int64_t>(A) * ne_b) +
                      static_cast<int64_t>(g) * (static_cast<int64_t>(kBlockCost) * nb + A);
   const int64_t pos0 = u0 + A;
   auto vr = [&](int64_t r) -> int64_t { return (r * V) / R; };   // start cost of range r
