@@ -21,7 +21,7 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ tables, int max_
                                     const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ positions,
                                     int32_t offset, int64_t n_tokens, int64_t* __restrict__ slots,
                                     int32_t* err) {
-  pdl_wait_and_release();
+  pdl_wait_and_release();   // (writes only the slots, which no kernel reads before its wait)
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n_tokens) return;
   const int64_t b = seq_idx ? seq_idx[t] : t;
@@ -50,7 +50,7 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
                                  const int64_t* __restrict__ slots, int64_t n_tokens, uint4* __restrict__ k_cache,
                                  uint4* __restrict__ v_cache, int64_t num_slots, int n_heads, int chunks_per_row,
                                  int32_t* err) {
-  pdl_wait_and_release();
+  pdl_wait();   // (writes the cache: no early release of the next launch)
   const int64_t per_kv = n_tokens * n_heads * chunks_per_row;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= 2 * per_kv) return;
@@ -82,7 +82,7 @@ __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint
                                      uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
                                      const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                                      int64_t num_slots, int n_heads, int chunks_per_row, int32_t* err) {
-  pdl_wait_and_release();
+  pdl_wait();   // (writes the cache: no early release of the next launch)
   const int64_t per_kv = n_tokens * n_heads * chunks_per_row;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= 2 * per_kv) return;
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(32) copy_blocks_kernel(const int32_t* __restri
                                                          int32_t* err) {
   extern __shared__ __align__(128) unsigned char cp_smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(cp_smem + static_cast<size_t>(kCopyStages) * chunk);
-  pdl_wait_and_release();
+  pdl_wait();   // (writes the cache: no early release of the next launch)
   if (threadIdx.x != 0) return;
   for (int s = 0; s < kCopyStages; ++s) mbar_init(&full[s], 1);
   fence_mbar_init();

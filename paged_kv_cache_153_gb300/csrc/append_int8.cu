@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_int8_kernel(const void* k_
                                                                   float4* params, const int32_t* rows_used,
                                                                   int n_heads, int d) {
   __shared__ float2 scratch[kQThreads / 32];
-  pdl_wait_and_release();
+  pdl_wait();   // (writes the cache: no early release of the next launch)
   const int64_t slab = blockIdx.x;             // block * n_heads + head
   const int blk = static_cast<int>(slab / n_heads);
   const int n = rows_used ? min(max(rows_used[blk], 0), kBlockSize) : kBlockSize;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
   constexpr int kPer = 2 * kQPer;   // values per thread: 16 rows x 128 / 128
   __shared__ float2 scratch[8];
   __shared__ float2 lohi_out[2];
-  pdl_wait_and_release();
+  pdl_wait();   // (writes the cache: no early release of the next launch)
   const int64_t t = blockIdx.x / n_heads;
   const int h = static_cast<int>(blockIdx.x % n_heads);
   const int64_t s = slots[t];

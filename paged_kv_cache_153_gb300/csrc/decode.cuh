@@ -392,7 +392,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.n_kv_heads;
-  pdl_wait_and_release();
+  // Early start.  This launch may begin while the previous kernel on the
+  // stream still runs (when that kernel released it early).  Everything up to
+  // the consumers' wait below, and all of the producer warp's work, only READS
+  // inputs -- lengths, scales, tables, q and the cache -- which no kernel of
+  // this library that releases early writes (the append, copy and quantise
+  // kernels never release early).  Every global write (the new rows, slots,
+  // outputs, partials, prefixes) is made by the consumer warps after their
+  // wait for the previous kernel.  The combine kernel may launch at once.
+  pdl_release();
 
   // ---- 1. per-sequence block counts and their prefix (all threads) -------
   if (tid == 0) *abort_flag = 0;
@@ -456,11 +464,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   }
   __syncthreads();
   const int64_t W = static_cast<int64_t>(Hkv) * cum[p.batch];
-  if (blockIdx.x == 0 && p.ws_cum != nullptr)
-    for (int b = tid; b <= p.batch; b += blockDim.x) {
-      p.ws_cum[b] = cum[b];
-      p.ws_cum[p.batch + 1 + b] = ne[b];
-    }
+  if (warp < NW) {
+    pdl_wait();   // the previous kernel has completed and its writes are visible
+    if (blockIdx.x == 0 && p.ws_cum != nullptr)
+      for (int b = tid; b <= p.batch; b += NW * 32) {
+        p.ws_cum[b] = cum[b];
+        p.ws_cum[p.batch + 1 + b] = ne[b];
+      }
+  }
 
   const int64_t R = gridDim.x;
   const int A = p.unit_cost;

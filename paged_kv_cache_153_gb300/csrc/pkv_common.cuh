@@ -172,13 +172,18 @@ __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, 
 
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: kernels of one decode step are launched so
-// that the next kernel's launch overlaps this one's tail.  Every kernel waits
-// for its predecessor's completion (and memory) before it reads global data,
-// then lets its own successor start launching.
+// that the next kernel's launch overlaps this one's tail.  A kernel waits for
+// its predecessor's completion (and memory) before it touches global data the
+// predecessor may write, and lets its own successor start launching once that
+// is safe (pdl_release).  Kernels that write the KV cache, the block tables or
+// the lengths never release early: their successor starts at their
+// completion, so a decode kernel may read those inputs before its own wait.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_and_release() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_wait();
+  pdl_release();
 }
 
 // ---------------------------------------------------------------------------
