@@ -315,7 +315,13 @@ pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void
 /* ---------------------------------------------------------------------------
  * INT8 KV cache with per-block min-max scaling ("What a KV cache is ...",
  * section 3.3: q = round((k - k_min) / (k_max - k_min) * 255), two scalars
- * per block).  Codes are uint8 [num_blocks, num_kv_heads, 16, head_dim]; the
+ * per block).  Codes are uint8, num_blocks x num_kv_heads slabs of 16 x
+ * head_dim bytes.  A K slab holds the 16 rows in order, [16][head_dim].  A V
+ * slab is the same with head_dim 64; with head_dim 128 it is stored
+ * transposed, [128][16], and the 16 columns of a row hold tokens 0 1 8 9 2 3
+ * 10 11 4 5 12 13 6 7 14 15 (column c: token 2 (c / 4) + c % 2 +
+ * 8 ((c / 2) % 2)), the order in which the decode kernel's tensor-core
+ * consumer multiplies them (so it needs no transpose).  The
  * scalars are per (block, KV head) for K and for V, stored as float
  * [num_blocks, num_kv_heads, 4] = (k_min, k_max, v_min, v_max) (16-byte
  * aligned).  Encoding: float32 in the formula's order with IEEE rounding,

@@ -8,12 +8,28 @@
 // have code 0.  Appending a token re-quantises its block's rows so far: the
 // old codes are decoded as min + ((q * (max - min)) / 255), the new row added,
 // min / max taken again and every row encoded again.
+//
+// Layout.  K codes of a (block, head) slab are stored as the rows: [16][d].
+// With d = 128, V codes are stored transposed, [d][16], and the 16 columns of
+// a row hold the tokens in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15
+// (column c holds token 2 (c / 4) + c % 2 + 8 ((c / 2) % 2)): an 8 x 16-byte
+// ldmatrix of that slab hands each lane of the decode kernel's p . V tensor
+// core MMA exactly the four tokens of its A fragment, so no transpose is
+// needed there.  With d = 64, V is stored as the rows, like K.
 #include <cuda_runtime.h>
 
 #include "host_util.h"
 #include "pkv_common.cuh"
 
 namespace pkv {
+
+// byte offset, inside a V slab, of row r (token), column c (head_dim index),
+// i = r * d + c in the row layout (see the layout note above)
+__device__ __forceinline__ int v_code_index(int i, int d) {
+  if (d != 128) return i;
+  const int r = i >> 7, c = i & 127;
+  return c * kBlockSize + 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
+}
 
 constexpr int kQThreads = 256;
 constexpr int kQPer = 8;   // values per thread: 16 rows x 128 / 256
@@ -92,7 +108,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_int8_kernel(const void* k_
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
       const int i = threadIdx.x + k * kQThreads;
-      if (i < kBlockSize * d) dst[i] = (i < count) ? int8_code(x[k], mm.x, span) : 0;
+      if (i < kBlockSize * d) dst[which ? v_code_index(i, d) : i] = (i < count) ? int8_code(x[k], mm.x, span) : 0;
     }
     lohi[2 * which] = count > 0 ? mm.x : 0.f;
     lohi[2 * which + 1] = count > 0 ? mm.y : 0.f;
@@ -154,7 +170,7 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int i = ht + k * 128;
-    q[k] = (i < row * d) ? codes[i] : 0;
+    q[k] = (i < row * d) ? codes[which ? v_code_index(i, d) : i] : 0;
   }
   float x[kPer];
   float lo = INFINITY, hi = -INFINITY;
@@ -176,7 +192,7 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int i = ht + k * 128;
-    if (i < count) codes[i] = int8_code(x[k], mm.x, span);
+    if (i < count) codes[which ? v_code_index(i, d) : i] = int8_code(x[k], mm.x, span);
   }
   if (ht == 0) lohi_out[which] = mm;
   __syncthreads();

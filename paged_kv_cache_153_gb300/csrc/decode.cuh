@@ -204,8 +204,12 @@ struct DecodeTraits {
   static constexpr int kNV = kTPG * G;                         // partial scores per lane
   static constexpr int kNF = (kNV >= kLPT) ? kNV / kLPT : 1;   // held scores after reduce-scatter
   static_assert(kNF == (G >= 2 ? G / 2 : 1), "lane/head mapping");
-  static_assert(!MMA || (G >= 2 && G <= 8 && (D * kEsz) % 128 == 0 && (kEsz == 2 || D * kEsz == 128)),
+  static_assert(!MMA || ((G >= 2 || std::is_same<KV, U8>::value) && G <= 8 && (D * kEsz) % 128 == 0 &&
+                          (kEsz == 2 || D * kEsz == 128)),
                 "tensor-core variant");
+  // INT8 through the tensor cores: V slabs are stored transposed ([d][16]
+  // token columns, see append_int8.cu) and staged by a plain 1-D copy
+  static constexpr bool kVT = MMA && std::is_same<KV, U8>::value;
 
   // shared memory layout (byte offsets from a 1024-byte aligned base)
   static __host__ __device__ size_t q_off(int stages) { return static_cast<size_t>(stages) * kStage; }
@@ -671,9 +675,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 #pragma unroll
                   for (int t = 0; t < T::kSubTiles; ++t) {
                     tma_load_2d(dst + t * 2048, &p.tmap_k, t * (128 / T::kEsz), y, &full_bar[s], pol_stream);
-                    tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
-                                pol_stream);
+                    if constexpr (!T::kVT)
+                      tma_load_2d(dst + T::kSlab + t * 2048, &p.tmap_v, t * (128 / T::kEsz), y, &full_bar[s],
+                                  pol_stream);
                   }
+                  if constexpr (T::kVT)
+                    bulk_g2s(dst + T::kSlab, vbase + (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab,
+                             T::kSlab, &full_bar[s], pol_stream);
                 } else {
                   const int64_t slab = (static_cast<int64_t>(ids) * p.block_heads + g) * T::kSlab;
                   bulk_g2s(dst, kbase + slab, T::kSlab, &full_bar[s], pol_stream);
@@ -828,7 +836,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                                               static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
                                               scales[Hkv + d.g], lane);
         }
-        if (n_valid > 0 && n_valid < kBlockSize) clear_rows<D, T::kEsz, true>(vslab, n_valid, lane);
+        // (INT8 codes are finite: a zero p needs no cleared row)
+        if constexpr (!kInt8)
+          if (n_valid > 0 && n_valid < kBlockSize) clear_rows<D, T::kEsz, true>(vslab, n_valid, lane);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (kFp8) {
 #pragma unroll
@@ -923,7 +933,25 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
           }
         }
-        if constexpr (kFp8) {
+        if constexpr (T::kVT) {
+          // INT8 V stored transposed: rows d = 32 cp + lane of the slab are
+          // the four 8-row matrices of two m-tiles; lane (r4, q4) gets the
+          // codes of columns 4 q4 .. 4 q4 + 3 of its row, which hold tokens
+          // 2 q4, 2 q4 + 1 (the A fragment's k, k + 1, paired with b0) and
+          // 2 q4 + 8, 2 q4 + 9 (paired with b1); rows in natural d order
+#pragma unroll
+          for (int cp = 0; cp < KS / 2; ++cp) {
+            uint32_t r[4];
+            ldsm_x4(vslab + (32 * cp + lane) * 16, r);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t a[4] = {byte2_to_f16x2(r[2 * h2], KV{}), byte2_to_f16x2(r[2 * h2 + 1], KV{}),
+                                     byte2_to_f16x2(r[2 * h2] >> 16, KV{}),
+                                     byte2_to_f16x2(r[2 * h2 + 1] >> 16, KV{})};
+              mma16816(o[2 * cp + h2], a, b0, b1, F16{});
+            }
+          }
+        } else if constexpr (kFp8) {
           // V rows converted to f16 and transposed in registers: m-tile c's row
           // r < 8 is d = 16c + 4(r/2) + r%2, row r + 8 is that d + 2
 #pragma unroll
@@ -969,20 +997,26 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         }
       }
       if (h0 < G) {
+        constexpr bool kPermD = kFp8 && !T::kVT;   // E4M3 / E5M2 V rows come out permuted
+        const bool two = h0 + 1 < G;                // (G = 1: the second column holds no head)
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d_lo = kFp8 ? 16 * mt + 4 * (r4 >> 1) + (r4 & 1) : 16 * mt + r4;
-          const int d_hi = kFp8 ? d_lo + 2 : d_lo + 8;
+          const int d_lo = kPermD ? 16 * mt + 4 * (r4 >> 1) + (r4 & 1) : 16 * mt + r4;
+          const int d_hi = kPermD ? d_lo + 2 : d_lo + 8;
           mw[h0 * D + d_lo] = o[mt][0];
-          mw[(h0 + 1) * D + d_lo] = o[mt][1];
           mw[h0 * D + d_hi] = o[mt][2];
-          mw[(h0 + 1) * D + d_hi] = o[mt][3];
+          if (two) {
+            mw[(h0 + 1) * D + d_lo] = o[mt][1];
+            mw[(h0 + 1) * D + d_hi] = o[mt][3];
+          }
         }
         if (r4 == 0) {
           mw[G * D + h0] = m0;
-          mw[G * D + h0 + 1] = m1;
           mw[G * D + G + h0] = l0;
-          mw[G * D + G + h0 + 1] = l1;
+          if (two) {
+            mw[G * D + h0 + 1] = m1;
+            mw[G * D + G + h0 + 1] = l1;
+          }
         }
       }
     } else {
@@ -1046,7 +1080,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
                                                static_cast<const unsigned char*>(p.v_new) + nr, scales[d.g],
                                                scales[Hkv + d.g], lane);
         }
-        if (n_valid > 0 && n_valid < kBlockSize) clear_rows<D, T::kEsz, false>(smem_u32(vslab), n_valid, lane);
+        if constexpr (!kInt8)   // (INT8 codes are finite: a zero p needs no cleared row)
+          if (n_valid > 0 && n_valid < kBlockSize) clear_rows<D, T::kEsz, false>(smem_u32(vslab), n_valid, lane);
 
         // ---- scores: partial dot products over this lane's 8 elements ----
         float part[T::kNV];

@@ -147,10 +147,13 @@ constexpr int kMmaWarps = 4;    // consumer warps of the tensor-core variant
 
 // G = 1 uses the CUDA-core consumer; G >= 2 over a 16-bit cache, or over a
 // one-byte (E4M3, E5M2 or INT8) cache with 128-byte rows, uses the tensor-core
-// consumer (the q-group times a 16-token block is an MMA tile).
+// consumer (the q-group times a 16-token block is an MMA tile), and so does
+// an INT8 cache with 128-byte rows at G = 1.
 template <typename QT, typename KV, int D, int G>
 DecodeLauncher pick_variant() {
-  if constexpr (G >= 2 && (KV::kBytes == 2 || D * KV::kBytes == 128))
+  // (an INT8 cache with 128-byte rows takes the tensor-core consumer for every
+  // group size: its V slabs are stored transposed for that consumer)
+  if constexpr ((G >= 2 || std::is_same<KV, U8>::value) && (KV::kBytes == 2 || D * KV::kBytes == 128))
     return launch_decode_variant<QT, KV, D, G, kMmaWarps, true>;
   else
     return launch_decode_variant<QT, KV, D, G, kCoreWarps, false>;

@@ -65,8 +65,7 @@ def test_quantize_bit_exact(pkv, dtype, hkv, d):
         kc, vc, prm = _quantize(pkv, w, ru)
         torch.cuda.synchronize()
         kq, vq, op = _oracle_quantize(w, ru)
-        assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(vc.cpu().numpy(), vq)
-        assert np.array_equal(prm.cpu().numpy(), op)
+        _same_codes(kc, vc, prm, kq, vq, op)
 
 
 def test_append_requantises_bit_exact(pkv):
@@ -90,8 +89,7 @@ def test_append_requantises_bit_exact(pkv):
             oi.append_row(kq, kp, int(s) // 16, h, int(s) % 16, kn[t, h])
             oi.append_row(vq, vp, int(s) // 16, h, int(s) % 16, vn[t, h])
     assert int(err.item()) == 0
-    assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(vc.cpu().numpy(), vq)
-    assert np.array_equal(prm.cpu().numpy(), np.concatenate([kp, vp], axis=2))
+    _same_codes(kc, vc, prm, kq, vq, np.concatenate([kp, vp], axis=2))
 
 
 def _oracle_attention(w, kq, vq, prm, seqs=None):
@@ -115,8 +113,28 @@ def _oracle_attention(w, kq, vq, prm, seqs=None):
     return ref
 
 
+# With head_dim 128 the library stores a V slab transposed, [128][16], with
+# token r in column 4 ((r % 8) // 2) + 2 (r // 8) + r % 2 (its documented
+# layout); the oracle's codes are [16][head_dim].
+V_COLUMN_OF_TOKEN = np.array([4 * ((r % 8) // 2) + 2 * (r // 8) + r % 2 for r in range(16)])
+
+
+def _v_rows(vc: np.ndarray) -> np.ndarray:
+    """Device V codes in the oracle's [NB, H, 16, d] row layout."""
+    if vc.shape[-1] != 128:
+        return vc
+    nb, h = vc.shape[:2]
+    t = vc.reshape(nb, h, 128, 16)                 # [d][column]
+    return np.ascontiguousarray(t[:, :, :, V_COLUMN_OF_TOKEN].transpose(0, 1, 3, 2))
+
+
+def test_v_column_order_is_a_permutation():
+    assert sorted(V_COLUMN_OF_TOKEN.tolist()) == list(range(16))
+    assert V_COLUMN_OF_TOKEN.tolist()[:4] == [0, 1, 4, 5] and V_COLUMN_OF_TOKEN[8] == 2
+
+
 def _same_codes(kc, vc, prm, kq, vq, op):
-    assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(vc.cpu().numpy(), vq)
+    assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(_v_rows(vc.cpu().numpy()), vq)
     assert np.array_equal(prm.cpu().numpy(), op)
 
 
