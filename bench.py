@@ -651,11 +651,11 @@ def run_int8(args, rank: int, local_rank: int) -> dict | None:
     stream.synchronize()
 
     def step():
-        pkv.pkv_slot_mapping(tables, lens, slots, num_blocks=w.num_blocks, position_offset=-1, err_flag=err,
-                             stream=stream)
-        pkv.pkv_kv_append_int8(kn, vn, slots, kc, vc, prm, err_flag=err, stream=stream)
-        pkv.pkv_paged_decode_attention_int8(q, kc, vc, prm, tables, lens, out, scale=w.scale, max_context_len=max_ctx,
-                                            workspace=ws, err_flag=err, stream=stream)
+        # one call: the re-quantising append with its slots from the table, the decode (started early, waiting
+        # for the append before it reads the cache), then the combine
+        pkv.pkv_paged_decode_step_int8(q, kn, vn, kc, vc, prm, tables, lens, out, scale=w.scale,
+                                       max_context_len=max_ctx, workspace=ws, slot_mapping_out=slots, err_flag=err,
+                                       stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -681,13 +681,15 @@ def run_int8(args, rank: int, local_rank: int) -> dict | None:
         "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": dict(describe(w), workload=f"int8: the gqa8b shape with the KV cache as INT8 codes + per-(block, "
-                       "head) min-max scalars (bf16 q/out)", step="slot mapping + INT8 append (re-quantising the "
-                       "block) + INT8 paged decode attention (decode + combine)"),
+                       "head) min-max scalars (bf16 q/out)", step="pkv_paged_decode_step_int8: INT8 append "
+                       "(slots from the table, re-quantising the block) + INT8 paged decode attention (decode + "
+                       "combine)"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic("int8"), "kernel": "the step's four launches, average over the timed region",
+                     "traffic": ncu_traffic("int8"), "kernel": "pkv_paged_decode_step_int8 call (append, decode "
+                     "and combine launches), average over the timed region",
                      "algorithmic_bytes_per_launch": algo, "avg_launch_ms": per_ms,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth"},
-        "gpu_launches": 4 * args.steps, "clocks": clocks.summary(), "e2e": None,
+        "gpu_launches": 3 * args.steps, "clocks": clocks.summary(), "e2e": None,
     }
 
 

@@ -402,6 +402,29 @@ pkv_status pkv_step_graph_launch(pkv_step_graph* graph, void* stream);
 void pkv_step_graph_destroy(pkv_step_graph* graph);
 
 /* ---------------------------------------------------------------------------
+ * The INT8 decode step: for every sequence b, the new rows k_new[b] /
+ * v_new[b] (q_dtype, [batch, num_kv_heads, head_dim]) go to position
+ * p = context_lens[b] - 1 (slot written to slot_mapping_out[b] when not NULL;
+ * -1 for an empty context or an out-of-range table entry, which also records
+ * PKV_ERR_OOB) and rows 0..p % 16 of that block are re-quantised as
+ * pkv_kv_append_int8 does; then the attention of
+ * pkv_paged_decode_attention_int8 runs over the context_lens[b] tokens.  The
+ * same codes, scalars, slots and outputs as pkv_slot_mapping +
+ * pkv_kv_append_int8 + pkv_paged_decode_attention_int8, bit for bit, in three
+ * launches (append with the slots from the table, decode, combine) that
+ * overlap: the decode kernel starts while the append runs and waits for it
+ * before reading the cache.  The new row's block must belong to sequence b
+ * alone.  Other arguments as in pkv_paged_decode_attention_int8.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_step_int8(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
+                                      uint8_t* v_cache, float* slab_params, const int32_t* block_tables,
+                                      const int32_t* context_lens, int batch, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                      int max_context_len, float scale, void* out, pkv_dtype q_dtype,
+                                      int partition_tokens, int64_t* slot_mapping_out, void* workspace,
+                                      size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Host-side block pool ("Series 03 ...", sections 3.2-3.3; "What a KV cache
  * is ...", section 3.2): a preallocated set of block ids handed out on demand,
  * with reference counts for blocks shared by several block tables.  Policy: a

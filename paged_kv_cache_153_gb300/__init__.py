@@ -25,6 +25,7 @@ __all__ = [
     "pkv_copy_blocks", "pkv_prepare_append", "pkv_paged_prefill_attention", "pkv_paged_decode_step_layer",
     "StepGraph", "pkv_kv_quantize_int8", "pkv_kv_append_int8", "pkv_paged_decode_attention_int8",
     "pkv_kv_append_e5m2", "pkv_paged_decode_attention_e5m2", "pkv_paged_decode_step_e5m2",
+    "pkv_paged_decode_step_int8",
 ]
 
 PKV_F16 = 0
@@ -102,6 +103,8 @@ _SIGS = {
     "pkv_kv_append_int8": (_i, [_p, _p, _p, _i64, _p, _p, _p, _i64, _i, _i, _i, _i, _p, _p]),
     "pkv_paged_decode_attention_int8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
                                              _i, _p, _sz, _p, _p]),
+    "pkv_paged_decode_step_int8": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i,
+                                        _i, _p, _p, _sz, _p, _p]),
 }
 _PREFILL_SIG = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i, _f, _p, _i, _p, _p]
 for _name, (_res, _args) in _SIGS.items():
@@ -416,6 +419,19 @@ def pkv_paged_decode_attention_int8(q, k_cache, v_cache, slab_params, block_tabl
         q.shape[0], q.shape[1], hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale, _ptr(out),
         _dtype_code(q, q_dtype), partition_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(err_flag), _stream(stream)))
+
+
+def pkv_paged_decode_step_int8(q, k_new, v_new, k_cache, v_cache, slab_params, block_tables, context_lens, out, *,
+                               scale: float, max_context_len: int, workspace, partition_tokens: int = 0,
+                               slot_mapping_out=None, q_dtype=None, err_flag=None, stream=None) -> None:
+    """The INT8 decode step in one decode launch (head_dim 128): the new rows
+    are appended with re-quantisation of their blocks, then attention."""
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_paged_decode_step_int8", lib.pkv_paged_decode_step_int8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slab_params), _ptr(block_tables),
+        _ptr(context_lens), q.shape[0], q.shape[1], hkv, d, bs, block_tables.shape[1], nb, max_context_len, scale,
+        _ptr(out), _dtype_code(q, q_dtype), partition_tokens, _ptr(slot_mapping_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream)))
 
 
 def pkv_blocks_needed(num_tokens: int, block_size: int = 16) -> int:

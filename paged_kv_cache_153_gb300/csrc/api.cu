@@ -121,7 +121,7 @@ pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const 
                          pkv_dtype dtype, int partition_tokens, void* workspace, size_t workspace_bytes,
                          int32_t* err_flag, void* stream, const void* k_new = nullptr, const void* v_new = nullptr,
                          int64_t* slots_out = nullptr, int num_layers = 1, int layer = 0,
-                         const void* slab_params = nullptr) {
+                         const void* slab_params = nullptr, bool wait_first = false) {
   // kv_kind: 0 = 16-bit cache, 1 = E4M3 with per-head scales, 2 = INT8 with
   // per-(block, head) min-max parameters, 3 = E5M2 with per-head scales
   const bool fp8 = kv_kind == 1 || kv_kind == 3, int8 = kv_kind == 2;
@@ -196,6 +196,7 @@ pkv_status decode_common(int kv_kind, const void* q, const void* k_cache, const 
   // (-1: the launched variant's default cost per (sequence, KV head))
   p.unit_cost = std::max(-1, std::min(1 << 16, env_int("PKV_UNIT_COST", -1)));
   p.slot_capacity = static_cast<int>(w.slots);
+  p.wait_first = wait_first ? 1 : 0;
   p.qk_scale_log2 = scale * kLog2e;
   // limit of each pipeline wait of the decode kernel: 1 s, or (for tests of
   // the timeout path) PKV_WAIT_LIMIT_NS nanoseconds
@@ -332,6 +333,33 @@ extern "C" pkv_status pkv_paged_decode_attention_int8(const void* q, const uint8
                        num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_context_len, scale,
                        out, q_dtype, partition_tokens, workspace, workspace_bytes, err_flag, stream, nullptr, nullptr,
                        nullptr, 1, 0, slab_params);
+}
+
+extern "C" pkv_status pkv_paged_decode_step_int8(const void* q, const void* k_new, const void* v_new,
+                                                 uint8_t* k_cache, uint8_t* v_cache, float* slab_params,
+                                                 const int32_t* block_tables, const int32_t* context_lens, int batch,
+                                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                                 int max_blocks_per_seq, int64_t num_blocks, int max_context_len,
+                                                 float scale, void* out, pkv_dtype q_dtype, int partition_tokens,
+                                                 int64_t* slot_mapping_out, void* workspace, size_t workspace_bytes,
+                                                 int32_t* err_flag, void* stream) {
+  // checks of pkv_kv_append_int8 and of the decode, before any launch
+  if (batch < 0 || num_kv_heads <= 0 || num_blocks < 0 || max_blocks_per_seq <= 0) return PKV_ERR_INVALID_ARG;
+  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slab_params || !block_tables || !context_lens ||
+      (reinterpret_cast<uintptr_t>(slab_params) & 15u))
+    return PKV_ERR_INVALID_ARG;
+  const pkv_status st = launch_append_int8_step(k_new, v_new, k_cache, v_cache, slab_params, block_tables,
+                                                context_lens, batch, max_blocks_per_seq, num_blocks, num_kv_heads,
+                                                head_dim, q_dtype, slot_mapping_out, err_flag,
+                                                static_cast<cudaStream_t>(stream));
+  if (st != PKV_OK) return st;
+  return decode_common(2, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_context_len, scale,
+                       out, q_dtype, partition_tokens, workspace, workspace_bytes, err_flag, stream, nullptr, nullptr,
+                       nullptr, 1, 0, slab_params, true);
 }
 
 extern "C" pkv_status pkv_paged_decode_step_layer(const void* q, const void* k_new, const void* v_new,

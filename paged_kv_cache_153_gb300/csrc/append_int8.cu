@@ -28,22 +28,11 @@ namespace pkv {
 __device__ __forceinline__ int v_code_index(int i, int d) {
   if (d != 128) return i;
   const int r = i >> 7, c = i & 127;
-  return c * kBlockSize + 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
+  return c * kBlockSize + int8_vt_column(r);
 }
 
 constexpr int kQThreads = 256;
 constexpr int kQPer = 8;   // values per thread: 16 rows x 128 / 256
-
-__device__ __forceinline__ uint8_t int8_code(float x, float lo, float span) {
-  if (span == 0.f) return 0;
-  const float t = __fmul_rn(__fdiv_rn(__fsub_rn(x, lo), span), 255.f);
-  return static_cast<uint8_t>(fminf(fmaxf(rintf(t), 0.f), 255.f));
-}
-
-__device__ __forceinline__ float int8_decode_f32(uint8_t q, float lo, float hi) {
-  const float span = __fsub_rn(hi, lo);
-  return __fadd_rn(lo, __fdiv_rn(__fmul_rn(static_cast<float>(q), span), 255.f));
-}
 
 // block-wide min and max of one value per thread (NaN-free inputs)
 __device__ __forceinline__ float2 block_minmax(float lo, float hi, float2* scratch) {
@@ -136,26 +125,67 @@ __device__ __forceinline__ float2 half_minmax(float lo, float hi, float2* scratc
   return r;
 }
 
+// Where the decode step's new rows go when the slots come from the block
+// table: token b is sequence b's new token at position context_lens[b] - 1.
+struct TableSlots {
+  const int32_t* block_tables;   // [B, max_blocks_per_seq]
+  const int32_t* context_lens;   // [B]
+  int max_blocks_per_seq;
+  int64_t* slots_out;            // [B] slots written (nullable); -1 for none
+};
+
 // one thread block per (token, KV head): write the token's row and re-quantise
 // rows [0, row] of its block's K slab (threads 0-127) and V slab (128-255)
-// side by side
-template <typename IN>
+// side by side.  FROM_TABLE (the append of the INT8 decode step): the slot of
+// token b is found from the block table (position context_lens[b] - 1) and
+// reported, and the kernel does not wait for the previous kernel.  That
+// kernel is the combine of the previous step (or a kernel that never releases
+// early), which launched this one only after the previous decode kernel -- the
+// last reader of these slabs -- had completed; the combine neither reads nor
+// writes the cache.  The next launch, the step's decode kernel, may start at
+// once: it waits for this grid before it reads the cache.
+template <typename IN, bool FROM_TABLE>
 __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_new, const void* v_new,
                                                                 const int64_t* slots, uint8_t* k_codes,
                                                                 uint8_t* v_codes, float4* params,
                                                                 int64_t num_slots, int n_heads, int d,
-                                                                int32_t* err) {
+                                                                int32_t* err, TableSlots ts) {
   constexpr int kPer = 2 * kQPer;   // values per thread: 16 rows x 128 / 128
   __shared__ float2 scratch[8];
   __shared__ float2 lohi_out[2];
-  pdl_wait();   // (writes the cache: no early release of the next launch)
+  if constexpr (FROM_TABLE)
+    pdl_release();
+  else
+    pdl_wait();   // (writes the cache: no early release of the next launch)
   const int64_t t = blockIdx.x / n_heads;
   const int h = static_cast<int>(blockIdx.x % n_heads);
-  const int64_t s = slots[t];
-  if (s < 0) return;
-  if (s >= num_slots) {
-    if (threadIdx.x == 0) record_error(err, PKV_ERR_OOB);
-    return;
+  int64_t s;
+  if constexpr (FROM_TABLE) {
+    // the slot-mapping rule: table[b][p / 16] * 16 + p % 16 for p = ctx - 1
+    const int p = ts.context_lens[t] - 1;
+    s = -1;
+    bool oob = false;
+    if (p >= 0) {
+      if (p / kBlockSize >= ts.max_blocks_per_seq) {
+        oob = true;
+      } else {
+        const int32_t phys = ts.block_tables[t * ts.max_blocks_per_seq + p / kBlockSize];
+        if (phys < 0 || static_cast<int64_t>(phys) * kBlockSize >= num_slots) oob = true;
+        else s = static_cast<int64_t>(phys) * kBlockSize + p % kBlockSize;
+      }
+    }
+    if (h == 0 && threadIdx.x == 0) {
+      if (ts.slots_out != nullptr) ts.slots_out[t] = s;
+      if (oob) record_error(err, PKV_ERR_OOB);
+    }
+    if (s < 0) return;
+  } else {
+    s = slots[t];
+    if (s < 0) return;
+    if (s >= num_slots) {
+      if (threadIdx.x == 0) record_error(err, PKV_ERR_OOB);
+      return;
+    }
   }
   const int which = threadIdx.x >> 7;   // 0: K, 1: V
   const int ht = threadIdx.x & 127;
@@ -236,10 +266,32 @@ extern "C" pkv_status pkv_kv_append_int8(const void* k_new, const void* v_new, c
       (reinterpret_cast<uintptr_t>(slab_params) & 15u))
     return PKV_ERR_INVALID_ARG;
   if (num_tokens * num_kv_heads > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  auto kern = in_dtype == PKV_F16 ? append_int8_kernel<F16> : append_int8_kernel<BF16>;
+  auto kern = in_dtype == PKV_F16 ? append_int8_kernel<F16, false> : append_int8_kernel<BF16, false>;
   const cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(num_tokens * num_kv_heads)), dim3(kQThreads), 0,
                                    static_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping, k_cache, v_cache,
                                    reinterpret_cast<float4*>(slab_params), num_blocks * kBlockSize, num_kv_heads,
-                                   head_dim, err_flag);
+                                   head_dim, err_flag, TableSlots{});
   return cuda_failed(e, "append_int8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
 }
+
+namespace pkv {
+
+// the append of the INT8 decode step: one new token per sequence at
+// position context_lens[b] - 1, slots from the block table (arguments checked
+// by the caller)
+pkv_status launch_append_int8_step(const void* k_new, const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
+                                   float* slab_params, const int32_t* block_tables, const int32_t* context_lens,
+                                   int batch, int max_blocks_per_seq, int64_t num_blocks, int num_kv_heads,
+                                   int head_dim, pkv_dtype in_dtype, int64_t* slots_out, int32_t* err_flag,
+                                   cudaStream_t stream) {
+  if (static_cast<int64_t>(batch) * num_kv_heads > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  auto kern = in_dtype == PKV_F16 ? append_int8_kernel<F16, true> : append_int8_kernel<BF16, true>;
+  const TableSlots ts{block_tables, context_lens, max_blocks_per_seq, slots_out};
+  const cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(batch * num_kv_heads)), dim3(kQThreads), 0,
+                                   stream, k_new, v_new, static_cast<const int64_t*>(nullptr), k_cache, v_cache,
+                                   reinterpret_cast<float4*>(slab_params), num_blocks * kBlockSize, num_kv_heads,
+                                   head_dim, err_flag, ts);
+  return cuda_failed(e, "append_int8_kernel launch") ? PKV_ERR_CUDA : PKV_OK;
+}
+
+}  // namespace pkv

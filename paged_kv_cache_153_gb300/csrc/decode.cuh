@@ -97,6 +97,8 @@ struct DecodeParams {
   int stages;                    // multiple of the consumer warp count
   float qk_scale_log2;           // softmax scale * log2(e)
   unsigned long long wait_limit_ns;   // limit of each pipeline wait (kWaitLimitNs unless overridden)
+  int wait_first;                // 1: the previous kernel writes the cache (the INT8 step's append), so the
+                                 // producer waits for it before its first read of the cache
 };
 
 struct SegDesc {
@@ -401,7 +403,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   // the consumers' wait below, and all of the producer warp's work, only READS
   // inputs -- lengths, scales, tables, q and the cache -- which no kernel of
   // this library that releases early writes (the append, copy and quantise
-  // kernels never release early).  Every global write (the new rows, slots,
+  // kernels never release early, except the INT8 step's own append, after
+  // which the producer waits first: wait_first).  Every global write (the new rows, slots,
   // outputs, partials, prefixes) is made by the consumer warps after their
   // wait for the previous kernel.  The combine kernel may launch at once.
   pdl_release();
@@ -531,6 +534,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 
   if (warp == NW) {
     // ======================= producer warp ===============================
+    if (p.wait_first) pdl_wait();
     const uint64_t pol_stream = policy_evict_first();
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);

@@ -7,6 +7,8 @@
 
 #include <utility>
 
+#include "../../include/pkv.h"
+
 namespace pkv {
 
 // Record a failed CUDA runtime call (name + error) for pkv_last_error() and
@@ -36,5 +38,14 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 bool encode_cache_tmap(CUtensorMap* map, const void* base, int64_t rows, int head_dim, int elt_bytes);
+
+// The append of the INT8 decode step (append_int8.cu): slots from the block
+// table, re-quantising append, early release of the decode launch that
+// follows (which waits for it before reading the cache).
+pkv_status launch_append_int8_step(const void* k_new, const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
+                                   float* slab_params, const int32_t* block_tables, const int32_t* context_lens,
+                                   int batch, int max_blocks_per_seq, int64_t num_blocks, int num_kv_heads,
+                                   int head_dim, pkv_dtype in_dtype, int64_t* slots_out, int32_t* err_flag,
+                                   cudaStream_t stream);
 
 }  // namespace pkv

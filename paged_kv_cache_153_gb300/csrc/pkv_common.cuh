@@ -312,6 +312,24 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, F16) {
   return r;
 }
 
+// INT8 per-block min-max codes: q = round((x - lo) / (hi - lo) * 255) in
+// float32 in that order (IEEE rounding, no contraction), half to even,
+// clamped to [0, 255]; hi == lo gives 0.  Decoding before a re-quantisation:
+// lo + ((q * (hi - lo)) / 255).
+__device__ __forceinline__ uint8_t int8_code(float x, float lo, float span) {
+  if (span == 0.f) return 0;
+  const float t = __fmul_rn(__fdiv_rn(__fsub_rn(x, lo), span), 255.f);
+  return static_cast<uint8_t>(fminf(fmaxf(rintf(t), 0.f), 255.f));
+}
+__device__ __forceinline__ float int8_decode_f32(uint32_t q, float lo, float hi) {
+  const float span = __fsub_rn(hi, lo);
+  return __fadd_rn(lo, __fdiv_rn(__fmul_rn(static_cast<float>(q), span), 255.f));
+}
+// column of token r (0..15) in a transposed INT8 V slab row (head_dim 128)
+__host__ __device__ __forceinline__ constexpr int int8_vt_column(int r) {
+  return 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
+}
+
 // fp32 -> output element, round to nearest even
 __device__ __forceinline__ __half to_out(float x, F16) { return __float2half_rn(x); }
 __device__ __forceinline__ __nv_bfloat16 to_out(float x, BF16) { return __float2bfloat16_rn(x); }

@@ -167,9 +167,10 @@ def test_attention(pkv, hq, hkv, d, dtype, partition):
 def test_full_size_int8_step_every_output(pkv):
     """The INT8 step exactly as the benchmark runs it, on the Llama-3-8B-shaped
     GQA workload (batch 64, 32 query / 8 KV heads, d 128, bf16, contexts
-    log-uniform in [128, 8192]): quantise the pool, then slot mapping,
-    re-quantising append and decode attention (decode + combine, balanced
-    split).  Codes, scalars and slots bit for bit; every output element."""
+    log-uniform in [128, 8192]): quantise the pool, then the fused step (slot
+    mapping, re-quantising append and decode attention in one decode launch,
+    then the combine; balanced split).  Codes, scalars and slots bit for bit;
+    every output element."""
     w = wl.make("gqa8b")
     d = gu.dev()
     kc, vc, prm = _quantize(pkv, w)
@@ -183,10 +184,8 @@ def test_full_size_int8_step_every_output(pkv):
     max_ctx = int(w.context_lens.max())
     ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
                                                     w.max_blocks_per_seq, max_ctx, 0), dtype=torch.uint8, device=d)
-    pkv.pkv_slot_mapping(tables, lens, slots, num_blocks=w.num_blocks, position_offset=-1, err_flag=err)
-    pkv.pkv_kv_append_int8(kn, vn, slots, kc, vc, prm, err_flag=err)
-    pkv.pkv_paged_decode_attention_int8(q, kc, vc, prm, tables, lens, out, scale=w.scale, max_context_len=max_ctx,
-                                        workspace=ws, err_flag=err)
+    pkv.pkv_paged_decode_step_int8(q, kn, vn, kc, vc, prm, tables, lens, out, scale=w.scale, max_context_len=max_ctx,
+                                   workspace=ws, slot_mapping_out=slots, err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     # oracle: the same append, row by row, on the oracle's codes
@@ -204,3 +203,77 @@ def test_full_size_int8_step_every_output(pkv):
     gu.record_parity("int8 (gqa8b shape)", split="balanced", max_abs=max_abs, max_rel=max_rel, elements=n,
                      bad=n_bad)
     assert n_bad == 0, f"{n_bad} of {n} elements beyond {INT8_ATOL} (max abs {max_abs:.3e})"
+
+
+def _int8_case(pkv, w, rows_used):
+    d = gu.dev()
+    kc, vc, prm = _quantize(pkv, w, rows_used)
+    tensors = dict(q=gu.bits_to_torch(w.q, w.dtype), kn=gu.bits_to_torch(w.k_new, w.dtype),
+                   vn=gu.bits_to_torch(w.v_new, w.dtype), tables=torch.from_numpy(w.block_tables).to(d),
+                   lens=torch.from_numpy(w.context_lens).to(d))
+    return kc, vc, prm, tensors
+
+
+def _rows_before_step(w):
+    """Rows of each block that hold tokens before the step: the last block of
+    each sequence holds (ctx - 1) % 16 rows, the others 16."""
+    rows = np.full(w.num_blocks, 16, dtype=np.int32)
+    for b, n in enumerate(w.context_lens):
+        if int(n) > 0:
+            rows[w.block_tables[b][(int(n) - 1) // 16]] = (int(n) - 1) % 16
+    return rows
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,partition", [(32, 8, 128, "bf16", 0), (16, 16, 128, "f16", 0),
+                                                      (16, 2, 128, "bf16", 32), (64, 8, 128, "bf16", 0),
+                                                      (8, 4, 64, "bf16", 0), (8, 8, 64, "f16", 16)])
+def test_fused_step_equals_the_three_calls(pkv, hq, hkv, d, dtype, partition):
+    # pkv_paged_decode_step_int8 (the append with its slots from the table,
+    # then the decode, which starts early and waits for it) gives the codes,
+    # scalars, slots and outputs of slot mapping + pkv_kv_append_int8 +
+    # pkv_paged_decode_attention_int8, bit for bit
+    lens = [1, 2, 15, 16, 17, 33, 100, 257, 1000, 0]
+    w = wl.build("int8fused", batch=len(lens), n_q_heads=hq, n_kv_heads=hkv, head_dim=d, dtype=dtype,
+                 kv_dtype=dtype, context_lens=lens, seed=hq + 5 * hkv + d)
+    rows = _rows_before_step(w)
+    dev = gu.dev()
+    ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.batch, hq, hkv, d, w.max_blocks_per_seq, max(lens),
+                                                    partition), dtype=torch.uint8, device=dev)
+    # three calls
+    kc1, vc1, prm1, t = _int8_case(pkv, w, rows)
+    slots1 = torch.empty(w.batch, dtype=torch.int64, device=dev)
+    out1 = torch.empty_like(t["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.pkv_slot_mapping(t["tables"], t["lens"], slots1, num_blocks=w.num_blocks, position_offset=-1, err_flag=err)
+    pkv.pkv_kv_append_int8(t["kn"], t["vn"], slots1, kc1, vc1, prm1, err_flag=err)
+    pkv.pkv_paged_decode_attention_int8(t["q"], kc1, vc1, prm1, t["tables"], t["lens"], out1, scale=w.scale,
+                                        max_context_len=max(lens), workspace=ws, partition_tokens=partition,
+                                        err_flag=err)
+    # one fused call
+    kc2, vc2, prm2, _ = _int8_case(pkv, w, rows)
+    slots2 = torch.full((w.batch,), -7, dtype=torch.int64, device=dev)
+    out2 = torch.empty_like(t["q"])
+    pkv.pkv_paged_decode_step_int8(t["q"], t["kn"], t["vn"], kc2, vc2, prm2, t["tables"], t["lens"], out2,
+                                   scale=w.scale, max_context_len=max(lens), workspace=ws,
+                                   partition_tokens=partition, slot_mapping_out=slots2, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(slots1, slots2)
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2) and torch.equal(prm1, prm2)
+    assert torch.equal(out1, out2)
+    # and the outputs match the oracle attending over the oracle's appended codes
+    kq, vq, op = _oracle_quantize(w, rows)
+    kp, vp = op[:, :, :2].copy(), op[:, :, 2:].copy()
+    knf, vnf = wl.bits_to_f32(w.k_new, dtype), wl.bits_to_f32(w.v_new, dtype)
+    for b, sl in enumerate(gu.oracle_slots(w)):
+        if sl < 0:
+            continue
+        for h in range(w.n_kv_heads):
+            oi.append_row(kq, kp, int(sl) // 16, h, int(sl) % 16, knf[b, h])
+            oi.append_row(vq, vp, int(sl) // 16, h, int(sl) % 16, vnf[b, h])
+    op = np.concatenate([kp, vp], axis=2)
+    _same_codes(kc2, vc2, prm2, kq, vq, op)
+    max_abs, _, n_bad, _ = gu.compare_all(out2, _oracle_attention(w, kq, vq, op), INT8_ATOL, 0.0)
+    assert n_bad == 0, max_abs
+
+
