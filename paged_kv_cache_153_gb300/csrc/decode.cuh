@@ -97,8 +97,9 @@ struct DecodeParams {
   int stages;                    // multiple of the consumer warp count
   float qk_scale_log2;           // softmax scale * log2(e)
   unsigned long long wait_limit_ns;   // limit of each pipeline wait (kWaitLimitNs unless overridden)
-  int wait_first;                // 1: the previous kernel writes the cache (the INT8 step's append), so the
-                                 // producer waits for it before its first read of the cache
+  int wait_first;                // 1: the previous kernel (the INT8 step's append) writes the last block of
+                                 // every (sequence, KV head): the producer waits for it before it loads such a
+                                 // block, the consumers before their first global write
 };
 
 struct SegDesc {
@@ -403,8 +404,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   // the consumers' wait below, and all of the producer warp's work, only READS
   // inputs -- lengths, scales, tables, q and the cache -- which no kernel of
   // this library that releases early writes (the append, copy and quantise
-  // kernels never release early, except the INT8 step's own append, after
-  // which the producer waits first: wait_first).  Every global write (the new rows, slots,
+  // kernels never release early, except the INT8 step's own append, which
+  // writes only the last block of each pair: the producer waits for it before
+  // it loads such a block, and the consumers before their first write --
+  // wait_first).  Every global write (the new rows, slots,
   // outputs, partials, prefixes) is made by the consumer warps after their
   // wait for the previous kernel.  The combine kernel may launch at once.
   pdl_release();
@@ -472,7 +475,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   __syncthreads();
   const int64_t W = static_cast<int64_t>(Hkv) * cum[p.batch];
   if (warp < NW) {
-    pdl_wait();   // the previous kernel has completed and its writes are visible
+    // the previous kernel has completed and its writes are visible (with
+    // wait_first, only thread block 0 waits here, for its prefixes; the
+    // others wait before their first output or partial)
+    if (!p.wait_first || blockIdx.x == 0) pdl_wait();
     if (blockIdx.x == 0 && p.ws_cum != nullptr)
       for (int b = tid; b <= p.batch; b += NW * 32) {
         p.ws_cum[b] = cum[b];
@@ -534,7 +540,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 
   if (warp == NW) {
     // ======================= producer warp ===============================
-    if (p.wait_first) pdl_wait();
     const uint64_t pol_stream = policy_evict_first();
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
@@ -660,6 +665,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             const uint32_t jw = kk / NW;                         // index in its warp's ring
             const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
             const uint32_t use = jw / SPW;
+            // (the INT8 step's append writes the last block of each pair: wait for it first)
+            if (p.wait_first && cur.i0 + w0 + lane == cur.nb - 1) pdl_wait();
             const bool stage_free = use == 0 || mbar_wait(&empty_bar[s], (use - 1) & 1, p.err, p.wait_limit_ns);
             if (!stage_free) {
               *abort_flag = 1;                                   // the stage is left as it is
@@ -1237,6 +1244,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
     }
 
     // ---- merge the NW warps' states and write the result ---------------------
+    if (p.wait_first) pdl_wait();   // (before the first global write; at once afterwards)
     named_bar_sync(1, NW * 32);
     const float vscale = scales[Hkv + d.g];
     for (int idx = tid; idx < G * D; idx += NW * 32) {
