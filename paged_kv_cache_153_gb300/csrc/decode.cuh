@@ -196,7 +196,8 @@ struct DecodeTraits {
   // INT8 caches also stage each block's 16-byte (k_min, k_max, v_min, v_max),
   // into a per-stage slot of its own (the K/V tiles stay 1024-byte aligned)
   static constexpr int kParam = std::is_same<KV, U8>::value ? 16 : 0;
-  static constexpr int kTx = 2 * kSlab + kParam;                 // bytes a stage receives
+  static constexpr int kTx = 2 * kSlab;                          // bytes a stage receives by TMA
+  // (an INT8 stage's scalars are stored into it by the issuing producer lane)
   static constexpr int kSubTiles = (D * kEsz) / 128;           // swizzled [16 x 128 B] tiles per slab
   static constexpr int kQBytes = G * D * 2;
   static constexpr int kThreads = (NW + 1) * 32;
@@ -659,6 +660,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       for (int w0 = 0; w0 < nseg && !stop; w0 += 32) {
         const int nxt_ids = (w0 + 32 < nseg) ? table_at(cur, w0 + 32) : (have_nxt ? table_at(nxt, 0) : 0);
         const int cnt = min(32, nseg - w0);
+        // INT8: each lane loads its block's (k_min, k_max, v_min, v_max) now,
+        // while the window is issued, and stores them into the stage itself
+        // (one TMA request fewer per block).  A last block written by the INT8
+        // step's append is read after the wait for it, below.
+        float4 prm_v = make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool last_blk = p.wait_first && cur.i0 + w0 + lane == cur.nb - 1;
+        if constexpr (T::kParam > 0)
+          if (lane < cnt && !last_blk && ids >= 0 && ids < p.num_blocks)
+            prm_v = __ldcg(p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g);
         for (int sb = 0; sb < cnt; sb += sub) {
           if (lane >= sb && lane < min(sb + sub, cnt) && !*abort_flag) {
             const uint32_t kk = k + lane;                        // CTA-local block counter
@@ -666,7 +676,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             const int s = static_cast<int>(kk % NW) + NW * static_cast<int>(jw % SPW);
             const uint32_t use = jw / SPW;
             // (the INT8 step's append writes the last block of each pair: wait for it first)
-            if (p.wait_first && cur.i0 + w0 + lane == cur.nb - 1) pdl_wait();
+            if (last_blk) {
+              pdl_wait();
+              if constexpr (T::kParam > 0)
+                if (ids >= 0 && ids < p.num_blocks)
+                  prm_v = __ldcg(p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g);
+            }
             const bool stage_free = use == 0 || mbar_wait(&empty_bar[s], (use - 1) & 1, p.err, p.wait_limit_ns);
             if (!stage_free) {
               *abort_flag = 1;                                   // the stage is left as it is
@@ -676,11 +691,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
               issued[s] = static_cast<int>(use);
               unsigned char* dst = ring + static_cast<size_t>(s) * T::kStage;
               if (ok) {
-                mbar_arrive_expect_tx(&full_bar[s], T::kTx);
+                // (the scalars' store is ordered before the consumer's read by
+                // this arrive, which releases; the stage was free)
                 if constexpr (T::kParam > 0)
-                  bulk_g2s(smem + T::prm_off(S) + s * T::kParam,
-                           p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g, T::kParam, &full_bar[s],
-                           pol_stream);
+                  *reinterpret_cast<float4*>(smem + T::prm_off(S) + s * T::kParam) = prm_v;
+                mbar_arrive_expect_tx(&full_bar[s], T::kTx);
                 if constexpr (MMA) {
                   const int y = (ids * p.block_heads + g) * kBlockSize;
 #pragma unroll
