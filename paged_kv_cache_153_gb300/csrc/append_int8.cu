@@ -138,12 +138,14 @@ struct TableSlots {
 // rows [0, row] of its block's K slab (threads 0-127) and V slab (128-255)
 // side by side.  FROM_TABLE (the append of the INT8 decode step): the slot of
 // token b is found from the block table (position context_lens[b] - 1) and
-// reported, and the kernel does not wait for the previous kernel.  That
-// kernel is the combine of the previous step (or a kernel that never releases
-// early), which launched this one only after the previous decode kernel -- the
-// last reader of these slabs -- had completed; the combine neither reads nor
-// writes the cache.  The next launch, the step's decode kernel, may start at
-// once: it waits for this grid before it reads the cache.
+// reported; the slab is read at once and written after the wait for the
+// previous kernel -- the previous step's combine, which may have released
+// this launch early and completes after the previous decode kernel, the last
+// reader of these slabs.  (The slabs were last written by the previous step's append,
+// which had completed before that decode kernel released its combine.)  The
+// next launch, the step's decode kernel, may start at once: it waits for this
+// grid before it reads a block this grid writes, and this grid completes only
+// after the previous kernel has.
 template <typename IN, bool FROM_TABLE>
 __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_new, const void* v_new,
                                                                 const int64_t* slots, uint8_t* k_codes,
@@ -178,7 +180,10 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
       if (ts.slots_out != nullptr) ts.slots_out[t] = s;
       if (oob) record_error(err, PKV_ERR_OOB);
     }
-    if (s < 0) return;
+    if (s < 0) {
+      pdl_wait();   // (every thread block waits: this grid completes after the previous one)
+      return;
+    }
   } else {
     s = slots[t];
     if (s < 0) return;
@@ -218,6 +223,7 @@ __global__ void __launch_bounds__(kQThreads) append_int8_kernel(const void* k_ne
   // (each thread rewrites only the codes it read, so no barrier is needed
   // between the reads and the writes)
   const float2 mm = half_minmax(lo, hi, scratch, which);
+  if constexpr (FROM_TABLE) pdl_wait();   // (the previous decode may still read this slab)
   const float span = __fsub_rn(mm.y, mm.x);
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {

@@ -97,6 +97,7 @@ struct DecodeParams {
   int stages;                    // multiple of the consumer warp count
   float qk_scale_log2;           // softmax scale * log2(e)
   unsigned long long wait_limit_ns;   // limit of each pipeline wait (kWaitLimitNs unless overridden)
+  int combine_early;             // 1: the combine releases the next launch at its start (else after its wait)
   int wait_first;                // 1: the previous kernel (the INT8 step's append) writes the last block of
                                  // every (sequence, KV head): the producer waits for it before it loads such a
                                  // block, the consumers before their first global write
@@ -410,8 +411,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   // it loads such a block, and the consumers before their first write --
   // wait_first).  Every global write (the new rows, slots,
   // outputs, partials, prefixes) is made by the consumer warps after their
-  // wait for the previous kernel.  The combine kernel may launch at once.
-  pdl_release();
+  // wait for the previous kernel.
+  //   The combine kernel is released early: at once when it releases its
+  // own successor only after its wait (combine_early = 0).  Otherwise -- the
+  // combine releases the next step's decode, whose producer reads the cache
+  // before its wait, or the next step's INT8 append, which reads the slabs
+  // that this step's append writes before its own wait, at once -- at once
+  // too, unless this launch appends the step's new rows (fused step: once
+  // those cache writes are fenced) or waits for such an append (wait_first:
+  // at the first return from the wait).
+  if (!p.combine_early || (p.k_new == nullptr && !p.wait_first)) pdl_release();
 
   // ---- 1. per-sequence block counts and their prefix (all threads) -------
   if (tid == 0) *abort_flag = 0;
@@ -537,6 +546,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       else if constexpr (!std::is_same<KV, U8>::value)   // (an INT8 cache has no fused append)
         *reinterpret_cast<uint2*>(dst) = quant8_fp8<KV>(&raw, is_v ? scales[Hkv + g] : scales[g], NT{});
     }
+    // every consumer's rows are in memory before any thread releases the
+    // combine (the first release of a thread block counts for all of it; the
+    // producer warp never releases)
+    __threadfence();
+    named_bar_sync(1, NW * 32);
+    pdl_release();
   }
 
   if (warp == NW) {
@@ -677,7 +692,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
             const uint32_t use = jw / SPW;
             // (the INT8 step's append writes the last block of each pair: wait for it first)
             if (last_blk) {
-              pdl_wait();
+              pdl_wait_and_release();
               if constexpr (T::kParam > 0)
                 if (ids >= 0 && ids < p.num_blocks)
                   prm_v = __ldcg(p.slab_params + static_cast<int64_t>(ids) * p.block_heads + g);
@@ -1259,7 +1274,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
     }
 
     // ---- merge the NW warps' states and write the result ---------------------
-    if (p.wait_first) pdl_wait();   // (before the first global write; at once afterwards)
+    if (p.wait_first) pdl_wait_and_release();   // (before the first global write; at once afterwards)
     named_bar_sync(1, NW * 32);
     const float vscale = scales[Hkv + d.g];
     for (int idx = tid; idx < G * D; idx += NW * 32) {
@@ -1330,6 +1345,12 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
   // the decode kernel clamps them; only the partials are then read after the
   // wait.  Otherwise the prefixes the decode kernel leaves in the workspace
   // are read after the wait.
+  //   The next launch is released at once (combine_early), or after the
+  // wait below: it is the next step's decode kernel (or INT8 append), which
+  // reads only inputs before its own wait and writes -- the cache, the
+  // workspace, the outputs -- only after it, that is after this grid (and so
+  // the decode grid before it) has completed.
+  if (p.combine_early) pdl_release();
   int64_t c0, ne_b, tot, tot_ne;
   int nb;
   if (!WIDE && p.batch <= kCombineLocalPrefix) {

@@ -68,28 +68,20 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
                         std::min<int64_t>(p.max_blocks_per_seq, p.max_nblk);
   // Resident blocks per SM (li.max_ctas_per_sm overrides), measured best on
   // GB300: 3 for one-byte caches through the tensor cores, whose per-block
-  // conversions want more consumer warps; for 16-bit caches through the tensor
-  // cores, 3 when the work could give each of them at least kBigWorkPerCta
-  // blocks (the mixed-length 64-sequence batch: 79.4 -> 77.4 us), else 2, where
-  // the per-block set-up of a third block costs more than it hides (the
-  // 16-sequence shared-prefix batch: 22.3 -> 23.2 us); 2 for the CUDA-core
-  // consumer, where a deeper stage ring per block beats more consumer warps.
-  constexpr int64_t kBigWorkPerCta = 128;
-  const bool big = w_max >= kBigWorkPerCta * 3 * li.num_sms;
-  const int want = li.max_ctas_per_sm > 0 ? li.max_ctas_per_sm
-                   : !MMA                 ? 2
-                   : Tr::kEsz == 1        ? 3
-                   : big                  ? 3
-                                          : 2;
+  // conversions want more consumer warps; 2 for 16-bit caches, where a deeper
+  // stage ring per block beats more consumer warps (with the combine released
+  // early, below: the mixed-length 64-sequence GQA batch 76.1 us at 2 against
+  // 77.4 at 3).
+  const int want = li.max_ctas_per_sm > 0 ? li.max_ctas_per_sm : (MMA && Tr::kEsz == 1) ? 3 : 2;
   // Cost of one (sequence, KV head) in the balanced split, in quarter blocks:
   // the per-segment work (query load, cross-warp merge, output or partial
   // write) and the consumer warps left idle by short segments.  Measured on
   // GB300 with mixed context lengths: 24 (6 blocks' worth of streaming) for
   // the CUDA-core consumer; 48 for the tensor-core one over one-byte caches,
-  // whose per-segment set-up is larger (INT8 60.9 -> 59.0 us against 24); over
-  // 16-bit caches 32 at 2 blocks per SM and 16 at 3 (sweeps of 8..48 on the
-  // two GQA batches above).
-  if (p.unit_cost < 0) p.unit_cost = !MMA ? 24 : Tr::kEsz == 1 ? 48 : want >= 3 ? 16 : 32;
+  // whose per-segment set-up is larger (INT8 60.9 -> 59.0 us against 24); 32
+  // for the tensor-core one over 16-bit caches (sweeps of 8..48 on the GQA
+  // batch above and on a 16-sequence shared-prefix batch).
+  if (p.unit_cost < 0) p.unit_cost = !MMA ? 24 : Tr::kEsz == 1 ? 48 : 32;
   occ = std::min(occ, want);
   int spw = 1;
   if (li.stages > 0) {
@@ -117,10 +109,22 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
   // a small workload (upper bound on blocks known from max_context_len) needs
   // no more than one thread block per few blocks of work
   if (p.part_blocks == 0) {
+    const int64_t w_max = static_cast<int64_t>(p.batch) * p.n_kv_heads *
+                          std::min<int64_t>(p.max_blocks_per_seq, p.max_nblk);
     grid = static_cast<int>(std::min<int64_t>(grid, std::max<int64_t>(1, (w_max + 3) / 4)));
   }
   if (grid < 1) grid = 1;
   p.stages = stages;
+  // The combine releases the next launch before its own wait when at most
+  // two decode blocks share each SM of a full grid (its small thread blocks
+  // then become resident beside them at once): the next step's decode kernel
+  // starts streaming during this one's tail.  With three per SM the
+  // combine's blocks get an SM only as decode blocks leave, and an early
+  // release measured far slower on GB300 (the 64-sequence GQA batch 111 us
+  // against 77); a grid smaller than the GPU has no tail to overlap (4 short
+  // sequences: 9.65 us against 9.28).  There the combine releases after its
+  // wait.
+  p.combine_early = (occ <= 2 && grid == li.num_sms * occ) ? 1 : 0;
   li.grid = grid;
   li.stages = stages;
   if constexpr (MMA) {

@@ -174,10 +174,11 @@ __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, 
 // programmatic dependent launch: kernels of one decode step are launched so
 // that the next kernel's launch overlaps this one's tail.  A kernel waits for
 // its predecessor's completion (and memory) before it touches global data the
-// predecessor may write, and lets its own successor start launching once that
-// is safe (pdl_release).  Kernels that write the KV cache, the block tables or
-// the lengths never release early: their successor starts at their
-// completion, so a decode kernel may read those inputs before its own wait.
+// predecessor may read or write, and lets its own successor start launching
+// once that is safe (pdl_release).  A kernel that writes the KV cache, the
+// block tables or the lengths releases its successor only after those writes
+// are fenced (or not at all: then at its completion), so a decode kernel may
+// read those inputs before its own wait.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
