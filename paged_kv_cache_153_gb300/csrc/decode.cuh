@@ -1317,11 +1317,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 // time), then the group combines its states with xor shuffles.  (b, g) pairs
 // written directly by the decode kernel are skipped.
 // ---------------------------------------------------------------------------
-// WIDE: 8 lanes per output quad (4 when that exceeds 1024 threads) for
-// (sequence, KV head) pairs split into many pieces; else one lane per quad.
+// WIDE: up to 8 lanes per output quad, at most 512 threads, for (sequence,
+// KV head) pairs split into many pieces; else one lane per quad.  (A thread
+// block of 1024 threads at 64 registers holds a whole SM's register file:
+// the 256 pairs of a 32-sequence batch then ran in two waves, and the
+// combine took 10.6 us of a 90.7 us long-context FP8 step on GB300.)
 template <int D, int G, bool WIDE>
 __host__ __device__ constexpr int combine_split() {
-  return !WIDE ? 1 : ((G * D / 4) * 8 <= 1024 ? 8 : 4);
+  return !WIDE ? 1 : (512 / (G * D / 4) >= 8 ? 8 : 512 / (G * D / 4) >= 1 ? 512 / (G * D / 4) : 1);
 }
 template <int D, int G, bool WIDE>
 __host__ __device__ constexpr int combine_threads() {
