@@ -1310,6 +1310,60 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 }
 
 // ---------------------------------------------------------------------------
+// Where the partials of a (sequence, KV head) pair lie, from the pair's
+// geometry: c0 / ne_b blocks and non-empty sequences before sequence b, tot /
+// tot_ne in all, nb blocks of b.  Ranges r0..r1 hold its blocks; its first
+// piece is in slot 2 r0 when its first block opens range r0, else 2 r0 + 1;
+// every later piece is in slot 2 r of its range r (the range's first segment).
+// ---------------------------------------------------------------------------
+struct CombineSpan {
+  int64_t r0, r1;
+  bool first_is_head;
+  int64_t pos0, V, W;            // balanced: cost of the first block, total cost; partition: flat blocks
+};
+
+__device__ __forceinline__ CombineSpan combine_span(const DecodeParams& p, int g, int64_t c0, int nb, int64_t tot,
+                                                    int64_t ne_b, int64_t tot_ne, int64_t R) {
+  const int Hkv = p.n_kv_heads;
+  CombineSpan s;
+  s.W = static_cast<int64_t>(Hkv) * tot;
+  const int64_t S0 = static_cast<int64_t>(Hkv) * c0 + static_cast<int64_t>(g) * nb;
+  // Balanced mode works on the cost axis (see blocks_before_cost): u0 is the
+  // cost where (b, g) starts, pos0 that of its first block; the block before
+  // S0, if any, is the last of the previous non-empty pair, at u0 - kBlockCost.
+  const int A = p.unit_cost;
+  s.V = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * tot + static_cast<int64_t>(A) * tot_ne);
+  const int64_t u0 = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * c0 + static_cast<int64_t>(A) * ne_b) +
+                     static_cast<int64_t>(g) * (static_cast<int64_t>(kBlockCost) * nb + A);
+  s.pos0 = u0 + A;
+  if (p.part_blocks) {
+    s.r0 = part_range_of(S0, s.W, R, p.part_blocks);
+    s.r1 = part_range_of(S0 + nb - 1, s.W, R, p.part_blocks);
+    s.first_is_head = (S0 == part_range_start(s.r0, s.W, R, p.part_blocks));
+  } else {
+    s.r0 = ((s.pos0 + 1) * R + s.V - 1) / s.V - 1;   // largest r with floor(r V / R) <= pos0
+    const int64_t posl = s.pos0 + static_cast<int64_t>(kBlockCost) * (nb - 1);
+    s.r1 = ((posl + 1) * R + s.V - 1) / s.V - 1;
+    s.first_is_head = (S0 == 0) || ((s.r0 * s.V) / R > u0 - kBlockCost);
+  }
+  return s;
+}
+
+// range r of [r0, r1] holds a block of the pair unless it is narrower than a
+// block (fewer blocks than ranges)
+__device__ __forceinline__ bool combine_has_piece(const CombineSpan& s, const DecodeParams& p, int64_t r, int64_t R) {
+  if (p.part_blocks)
+    return part_range_start(r + 1, s.W, R, p.part_blocks) > part_range_start(r, s.W, R, p.part_blocks);
+  if (r == s.r0) return true;
+  const int64_t i = ((r * s.V) / R - s.pos0 + kBlockCost - 1) / kBlockCost;
+  return s.pos0 + static_cast<int64_t>(kBlockCost) * i < ((r + 1) * s.V) / R;
+}
+
+__device__ __forceinline__ int64_t combine_slot(const CombineSpan& s, int64_t r) {
+  return (r == s.r0 && !s.first_is_head) ? 2 * r + 1 : 2 * r;
+}
+
+// ---------------------------------------------------------------------------
 // combine: out[b, g*G + h] = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r over
 // the partial slots of (b, g); zeros for an empty context.  One thread block
 // per (b, g).  Each group of kSplit adjacent lanes owns 4 consecutive outputs;
@@ -1403,45 +1457,13 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
     if (live_t && sub == 0) store4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int Hkv = p.n_kv_heads;
-  const int64_t W = static_cast<int64_t>(Hkv) * tot;
-  const int64_t S0 = static_cast<int64_t>(Hkv) * c0 + static_cast<int64_t>(g) * nb;
   const int64_t R = grid_ranges;
-  // Balanced mode works on the cost axis (see blocks_before_cost): u0 is the
-  // cost where (b, g) starts, pos0 that of its first block; the block before
-  // S0, if any, is the last of the previous non-empty pair, at u0 - kBlockCost.
-  const int A = p.unit_cost;
-  const int64_t V = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * tot +
-                                                 static_cast<int64_t>(A) * tot_ne);
-  const int64_t u0 = static_cast<int64_t>(Hkv) * (static_cast<int64_t>(kBlockCost) * c0 +
-                                                  static_cast<int64_t>(A) * ne_b) +
-                     static_cast<int64_t>(g) * (static_cast<int64_t>(kBlockCost) * nb + A);
-  const int64_t pos0 = u0 + A;
-  auto vr = [&](int64_t r) -> int64_t { return (r * V) / R; };   // start cost of range r
-  int64_t r0, r1;
-  bool first_is_head;
-  if (p.part_blocks) {
-    r0 = part_range_of(S0, W, R, p.part_blocks);
-    r1 = part_range_of(S0 + nb - 1, W, R, p.part_blocks);
-    first_is_head = (S0 == part_range_start(r0, W, R, p.part_blocks));
-  } else {
-    r0 = ((pos0 + 1) * R + V - 1) / V - 1;   // largest r with vr(r) <= pos0
-    const int64_t posl = pos0 + static_cast<int64_t>(kBlockCost) * (nb - 1);
-    r1 = ((posl + 1) * R + V - 1) / V - 1;
-    first_is_head = (S0 == 0) || (vr(r0) > u0 - kBlockCost);
-  }
-  if (r0 == r1) return;   // one segment: written by the decode kernel
-  // a range after r0 holds a block of (b, g) unless it is narrower than a block
-  auto has_piece = [&](int64_t r) -> bool {
-    if (p.part_blocks) return part_range_start(r + 1, W, R, p.part_blocks) > part_range_start(r, W, R, p.part_blocks);
-    if (r == r0) return true;
-    const int64_t i = (vr(r) - pos0 + kBlockCost - 1) / kBlockCost;
-    return pos0 + static_cast<int64_t>(kBlockCost) * i < vr(r + 1);
-  };
+  const CombineSpan sp = combine_span(p, g, c0, nb, tot, ne_b, tot_ne, R);
+  if (sp.r0 == sp.r1) return;   // one segment: written by the decode kernel
   const int h = live_t ? (4 * t) / D : 0, e = live_t ? (4 * t) % D : 0;
   float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
   constexpr int kBatch = WIDE ? 4 : 8;   // partials whose loads are issued together, per lane
-  for (int64_t rb = r0 + sub; rb <= r1; rb += kBatch * kSplit) {
+  for (int64_t rb = sp.r0 + sub; rb <= sp.r1; rb += kBatch * kSplit) {
     float2 ml[kBatch];
     float4 ov[kBatch];
 #pragma unroll
@@ -1449,8 +1471,8 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
       const int64_t r = rb + static_cast<int64_t>(q) * kSplit;
       // ranges between r0 and r1 may be empty (fewer blocks than ranges):
       // they wrote nothing for this (b, g)
-      const bool live = live_t && r <= r1 && has_piece(r);
-      const int64_t sl = (r == r0 && !first_is_head) ? 2 * r + 1 : 2 * r;
+      const bool live = live_t && r <= sp.r1 && combine_has_piece(sp, p, r, R);
+      const int64_t sl = combine_slot(sp, r);
       ml[q] = live ? *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2) : make_float2(-INFINITY, 0.f);
       ov[q] = live ? *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -1492,6 +1514,130 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
     store4(O0 * inv, O1 * inv, O2 * inv, O3 * inv);
   }
+}
+
+// ---------------------------------------------------------------------------
+// The narrow combine: one warp per (sequence, KV head) pair, kCombineWarps
+// pairs per thread block.  Lane l owns output quads l, l + 32, ... and merges
+// the pair's pieces into each in range order (the loads of kBatch pieces are
+// issued together).  The thread blocks are small and hold no shared memory,
+// so they become resident beside the decode grid as soon as they launch:
+// they sum the block counts from the context lengths (small batches) while
+// the decode grid runs and start on the partials the moment it completes.
+// ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 4;
+
+template <typename QT, int D, int G>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    paged_decode_combine_warps_kernel(const __grid_constant__ DecodeParams p, int grid_ranges) {
+  constexpr int kQuads = G * D / 4;
+  constexpr int kQPL = (kQuads + 31) / 32;          // output quads per lane
+  constexpr int kBatch = kQPL >= 8 ? 1 : kQPL >= 4 ? 2 : 4;   // pieces loaded together
+  const int lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kCombineWarps + static_cast<int>(threadIdx.x >> 5);
+  // (release: as in paged_decode_combine_kernel)
+  if (p.combine_early) pdl_release();
+  if (u >= p.batch * p.n_kv_heads) {
+    pdl_wait();   // (every warp waits: this grid completes after the decode grid)
+    return;
+  }
+  const int b = u / p.n_kv_heads, g = u % p.n_kv_heads;
+  int64_t c0, ne_b, tot, tot_ne;
+  int nb;
+  if (p.batch <= kCombineLocalPrefix) {
+    // the prefixes from the context lengths, clamped as the decode kernel
+    // clamps them, before the wait
+    long long v0 = 0, v1 = 0, v2 = 0, v3 = 0, v4 = 0;
+    for (int i = lane; i < p.batch; i += 32) {
+      const int ctx = p.context_lens[i];
+      const int n = ctx < 0 ? 0 : min((ctx + kBlockSize - 1) / kBlockSize, min(p.max_blocks_per_seq, p.max_nblk));
+      v2 += n;
+      v3 += n > 0;
+      if (i < b) {
+        v0 += n;
+        v1 += n > 0;
+      }
+      if (i == b) v4 = n;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+      v2 += __shfl_xor_sync(0xffffffffu, v2, o);
+      v3 += __shfl_xor_sync(0xffffffffu, v3, o);
+      v4 += __shfl_xor_sync(0xffffffffu, v4, o);
+    }
+    c0 = v0, ne_b = v1, tot = v2, tot_ne = v3;
+    nb = static_cast<int>(v4);
+    pdl_wait_and_release();
+  } else {
+    pdl_wait_and_release();
+    c0 = p.ws_cum[b];
+    nb = p.ws_cum[b + 1] - p.ws_cum[b];
+    tot = p.ws_cum[p.batch];
+    ne_b = p.ws_cum[p.batch + 1 + b];
+    tot_ne = p.ws_cum[2 * p.batch + 1];
+  }
+  auto* out = static_cast<typename QT::storage*>(p.out) + (static_cast<int64_t>(b) * p.n_q_heads + g * G) * D;
+  auto store4 = [&](int quad, float a, float b2, float c, float d) {
+    const uint32_t lo = pack2(a, b2, QT{}), hi = pack2(c, d, QT{});
+    *reinterpret_cast<uint2*>(out + 4 * quad) = make_uint2(lo, hi);
+  };
+  if (nb == 0) {
+#pragma unroll
+    for (int k = 0; k < kQPL; ++k)
+      if (lane + 32 * k < kQuads) store4(lane + 32 * k, 0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int64_t R = grid_ranges;
+  const CombineSpan sp = combine_span(p, g, c0, nb, tot, ne_b, tot_ne, R);
+  if (sp.r0 == sp.r1) return;   // one segment: written by the decode kernel
+  float M[kQPL], L[kQPL], O[kQPL][4];
+#pragma unroll
+  for (int k = 0; k < kQPL; ++k) {
+    M[k] = -INFINITY;
+    L[k] = 0.f;
+    O[k][0] = O[k][1] = O[k][2] = O[k][3] = 0.f;
+  }
+  for (int64_t rb = sp.r0; rb <= sp.r1; rb += kBatch) {
+    float2 ml[kBatch][kQPL];
+    float4 ov[kBatch][kQPL];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int64_t r = rb + q;
+      const bool live = r <= sp.r1 && combine_has_piece(sp, p, r, R);
+      const int64_t sl = combine_slot(sp, r);
+#pragma unroll
+      for (int k = 0; k < kQPL; ++k) {
+        const int quad = lane + 32 * k;
+        const bool lq = live && quad < kQuads;
+        const int h = lq ? (4 * quad) / D : 0, e = lq ? (4 * quad) % D : 0;
+        ml[q][k] = lq ? *reinterpret_cast<const float2*>(p.ws_ml + (sl * G + h) * 2) : make_float2(-INFINITY, 0.f);
+        ov[q][k] = lq ? *reinterpret_cast<const float4*>(p.ws_o + (sl * G + h) * D + e)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q)
+#pragma unroll
+      for (int k = 0; k < kQPL; ++k) {
+        const float mn = fmaxf(M[k], ml[q][k].x);
+        const float ref = (mn == -INFINITY) ? 0.f : mn;
+        const float a = exp2f(M[k] - ref), w = exp2f(ml[q][k].x - ref);
+        L[k] = L[k] * a + w * ml[q][k].y;
+        O[k][0] = O[k][0] * a + w * ov[q][k].x;
+        O[k][1] = O[k][1] * a + w * ov[q][k].y;
+        O[k][2] = O[k][2] * a + w * ov[q][k].z;
+        O[k][3] = O[k][3] * a + w * ov[q][k].w;
+        M[k] = mn;
+      }
+  }
+#pragma unroll
+  for (int k = 0; k < kQPL; ++k)
+    if (lane + 32 * k < kQuads) {
+      const float inv = (L[k] > 0.f) ? 1.f / L[k] : 0.f;
+      store4(lane + 32 * k, O[k][0] * inv, O[k][1] * inv, O[k][2] * inv, O[k][3] * inv);
+    }
 }
 
 }  // namespace pkv

@@ -145,8 +145,9 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
     const cudaError_t e =
         wide ? launch_pdl(paged_decode_combine_kernel<QT, D, G, true>, dim3(units),
                           dim3(combine_threads<D, G, true>()), 0, stream, p, grid)
-             : launch_pdl(paged_decode_combine_kernel<QT, D, G, false>, dim3(units),
-                          dim3(combine_threads<D, G, false>()), 0, stream, p, grid);
+             : launch_pdl(paged_decode_combine_warps_kernel<QT, D, G>,
+                          dim3((units + kCombineWarps - 1) / kCombineWarps), dim3(kCombineWarps * 32), 0, stream,
+                          p, grid);
     if (cuda_failed(e, "paged_decode_combine_kernel launch")) return PKV_ERR_CUDA;
   }
   return PKV_OK;
