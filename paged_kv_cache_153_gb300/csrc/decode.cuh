@@ -308,6 +308,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
 __device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, E4M3) { return e4m3x2_to_f16x2(w); }
 __device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, E5M2) { return e5m2x2_to_f16x2(w); }
 __device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t w, U8) { return __byte_perm(w, 0x64u, 0x4140u); }
+// the same for the two codes in bits 16-31 of w (no shift: the permute
+// selects bytes 2 and 3; the E4M3 conversion reads the upper half register)
+__device__ __forceinline__ uint32_t byte2_hi_to_f16x2(uint32_t w, E4M3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(r) : "r"(w));
+  return r;
+}
+__device__ __forceinline__ uint32_t byte2_hi_to_f16x2(uint32_t w, E5M2) { return __byte_perm(w, 0u, 0x3424u); }
+__device__ __forceinline__ uint32_t byte2_hi_to_f16x2(uint32_t w, U8) { return __byte_perm(w, 0x64u, 0x4342u); }
 
 
 // address of 16-byte chunk `chunk` of row `row` in a slab staged as 128B-swizzled
@@ -889,8 +898,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const uint32_t a[4] = {byte2_to_f16x2(r[2 * h2], KV{}), byte2_to_f16x2(r[2 * h2 + 1], KV{}),
-                                     byte2_to_f16x2(r[2 * h2] >> 16, KV{}),
-                                     byte2_to_f16x2(r[2 * h2 + 1] >> 16, KV{})};
+                                     byte2_hi_to_f16x2(r[2 * h2], KV{}),
+                                     byte2_hi_to_f16x2(r[2 * h2 + 1], KV{})};
               mma16816(c, a, bq[2 * cp + h2][0], bq[2 * cp + h2][1], F16{});
             }
           }
@@ -987,8 +996,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const uint32_t a[4] = {byte2_to_f16x2(r[2 * h2], KV{}), byte2_to_f16x2(r[2 * h2 + 1], KV{}),
-                                     byte2_to_f16x2(r[2 * h2] >> 16, KV{}),
-                                     byte2_to_f16x2(r[2 * h2 + 1] >> 16, KV{})};
+                                     byte2_hi_to_f16x2(r[2 * h2], KV{}),
+                                     byte2_hi_to_f16x2(r[2 * h2 + 1], KV{})};
               mma16816(o[2 * cp + h2], a, b0, b1, F16{});
             }
           }
@@ -1002,9 +1011,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const uint32_t a[4] = {movmatrix_trans(byte2_to_f16x2(r[2 * h2], KV{})),
-                                     movmatrix_trans(byte2_to_f16x2(r[2 * h2] >> 16, KV{})),
+                                     movmatrix_trans(byte2_hi_to_f16x2(r[2 * h2], KV{})),
                                      movmatrix_trans(byte2_to_f16x2(r[2 * h2 + 1], KV{})),
-                                     movmatrix_trans(byte2_to_f16x2(r[2 * h2 + 1] >> 16, KV{}))};
+                                     movmatrix_trans(byte2_hi_to_f16x2(r[2 * h2 + 1], KV{}))};
               mma16816(o[2 * cp + h2], a, b0, b1, F16{});
             }
           }
