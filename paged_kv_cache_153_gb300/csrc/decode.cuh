@@ -795,6 +795,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   const int mrow = lane & 7, mi = lane >> 3;      // ldmatrix: row within matrix, matrix index
   uint32_t j = 0;
   uint32_t k_base = 0;                   // CTA-local counter of the segment's first block
+  // This warp consumes CTA-local blocks warp, warp + NW, ... in turn, the
+  // j-th of them from stage warp + NW (j % SPW) at phase (j / SPW) & 1:
+  // js = j % SPW and ph are kept as running counters.
+  int js = 0;
+  uint32_t ph = 0;
   while (true) {
     const int qs = j & 1;
     const bool got = !*abort_flag && mbar_wait(&qfull_bar[qs], (j >> 1) & 1, p.err, p.wait_limit_ns);
@@ -845,8 +850,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       // INT8 cache: the MMAs see the codes as integers offset by 1024; a
       // score is dk (q . codes) + k_min sum(q) and p . V is
       // dv (p . codes) + v_min sum(p), the offset taken out of both sums
+      // (for p . V through a third MMA, of all-ones rows with the same p:
+      // its accumulator cz holds sum(f16(p dv)) per head, rescaled with o)
       constexpr bool kInt8 = T::kParam > 0;
-      float qs0 = 0.f, qs1 = 0.f, b0r = 0.f, b1r = 0.f;   // sum(q) of heads h0, h0 + 1; v_min sum(p)
+      float qs0 = 0.f, qs1 = 0.f, b0r = 0.f, b1r = 0.f;   // sc sum(q) of heads h0, h0 + 1; v_min sum(p)
+      float cz[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (kInt8) {
         float a = 0.f;
 #pragma unroll
@@ -856,8 +864,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         }
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);        // sum(q) of head r4
-        qs0 = __shfl_sync(0xffffffffu, a, 4 * h0);
-        qs1 = __shfl_sync(0xffffffffu, a, 4 * (h0 + 1) < 32 ? 4 * (h0 + 1) : 0);
+        qs0 = sc * __shfl_sync(0xffffffffu, a, 4 * h0);
+        qs1 = sc * __shfl_sync(0xffffffffu, a, 4 * (h0 + 1) < 32 ? 4 * (h0 + 1) : 0);
       }
       float o[KS][4];
 #pragma unroll
@@ -866,11 +874,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       const int krow = mrow + 8 * (mi & 1), kchunk = mi >> 1;   // A of q.K^T (and fp8 V)
       const int vrow = mrow + 8 * (mi >> 1), vchunk = mi & 1;   // A of p.V (16-bit transposed load)
       for (int ii = first; ii < nseg; ii += NW) {
-        const uint32_t kk = k_base + ii;
-        const uint32_t jw = kk / NW;
-        const int s = warp + NW * static_cast<int>(jw % SPW);
+        const int s = warp + NW * js;
         // (a warp vote: every lane of the warp takes the same decision)
-        const bool ready = !*abort_flag && mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err, p.wait_limit_ns);
+        const bool ready = !*abort_flag && mbar_wait(&full_bar[s], ph, p.err, p.wait_limit_ns);
+        if (++js == SPW) {
+          js = 0;
+          ph ^= 1u;
+        }
         if (!__all_sync(0xffffffffu, ready)) {
           *abort_flag = 1;
           break;
@@ -915,19 +925,26 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         if constexpr (kInt8) {
           const float4 prm = n_valid > 0 ? *reinterpret_cast<const float4*>(smem + T::prm_off(S) + s * T::kParam)
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          // the MMAs saw 1024 + code: dk (q . (1024 + codes)) + (k_min - 1024 dk) sum(q)
+          // the MMAs saw 1024 + code: dk (q . (1024 + codes)) + (k_min - 1024 dk) sum(q),
+          // times the score scale (folded into dk and into qs0, qs1)
           const float dk = (prm.y - prm.x) * (1.f / 255.f);
           dv = (prm.w - prm.z) * (1.f / 255.f);
           vmin = prm.z;
-          const float kmin = prm.x - 1024.f * dk;
-          c[0] = fmaf(c[0], dk, kmin * qs0);
-          c[1] = fmaf(c[1], dk, kmin * qs1);
-          c[2] = fmaf(c[2], dk, kmin * qs0);
-          c[3] = fmaf(c[3], dk, kmin * qs1);
+          const float kmin = prm.x - 1024.f * dk, dks = dk * sc;
+          const float k0 = kmin * qs0, k1 = kmin * qs1;
+          c[0] = fmaf(c[0], dks, k0);
+          c[1] = fmaf(c[1], dks, k1);
+          c[2] = fmaf(c[2], dks, k0);
+          c[3] = fmaf(c[3], dks, k1);
+        } else {
+          c[0] *= sc;
+          c[1] *= sc;
+          c[2] *= sc;
+          c[3] *= sc;
         }
         const bool v0 = r4 < n_valid, v1 = r4 + 8 < n_valid;
-        const float s00 = v0 ? c[0] * sc : -INFINITY, s01 = v0 ? c[1] * sc : -INFINITY;
-        const float s10 = v1 ? c[2] * sc : -INFINITY, s11 = v1 ? c[3] * sc : -INFINITY;
+        const float s00 = v0 ? c[0] : -INFINITY, s01 = v0 ? c[1] : -INFINITY;
+        const float s10 = v1 ? c[2] : -INFINITY, s11 = v1 ? c[3] : -INFINITY;
         float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
         for (int msk = 4; msk < 32; msk <<= 1) {
@@ -962,11 +979,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         l0 = l0 * a0 + ((p0.x + r0.x) + (p1.x + r1.x));
         l1 = l1 * a1 + ((p0.y + r0.y) + (p1.y + r1.y));
         if constexpr (kInt8) {
-          // the MMA adds 1024 f16(p dv) per key on top of f16(p dv) code: take
-          // exactly that out (from the packed values), and add v_min sum(p)
-          const float2 u0 = unpack2(x0, MT{}), u1 = unpack2(x1, MT{});
-          b0r = b0r * a0 + ((p0.x + p1.x) * vmin - 1024.f * (u0.x + u1.x));
-          b1r = b1r * a1 + ((p0.y + p1.y) * vmin - 1024.f * (u0.y + u1.y));
+          // v_min sum(p) (the MMA's 1024 f16(p dv) per key is taken out through cz)
+          b0r = b0r * a0 + (p0.x + p1.x) * vmin;
+          b1r = b1r * a1 + (p0.y + p1.y) * vmin;
         }
         const bool resc = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
         m0 = mn0;
@@ -982,6 +997,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
           for (int mt = 0; mt < KS; ++mt) {
             o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
           }
+          if constexpr (kInt8) {
+            cz[0] *= a0; cz[1] *= a1; cz[2] *= a0; cz[3] *= a1;
+          }
+        }
+        if constexpr (kInt8) {
+          constexpr uint32_t kOnes = 0x3C003C00u;   // f16 1.0 pairs
+          const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
+          mma16816(cz, ones, b0, b1, F16{});
         }
         if constexpr (T::kVT) {
           // INT8 V stored transposed: rows d = 32 cp + lane of the slab are
@@ -1041,9 +1064,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
         }
       }
       if constexpr (kInt8) {
+        // (cz is the same in every row: all-ones A)
+        const float t0 = fmaf(-1024.f, cz[0], b0r), t1 = fmaf(-1024.f, cz[1], b1r);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          o[mt][0] += b0r; o[mt][1] += b1r; o[mt][2] += b0r; o[mt][3] += b1r;
+          o[mt][0] += t0; o[mt][1] += t1; o[mt][2] += t0; o[mt][3] += t1;
         }
       }
       if (h0 < G) {
@@ -1110,11 +1135,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
       for (int x = 0; x < NF; ++x) l_part[x] = 0.f;
 
       for (int ii = first; ii < nseg; ii += NW) {
-        const uint32_t kk = k_base + ii;
-        const uint32_t jw = kk / NW;
-        const int s = warp + NW * static_cast<int>(jw % SPW);
+        const int s = warp + NW * js;
         // (a warp vote: every lane of the warp takes the same decision)
-        const bool ready = !*abort_flag && mbar_wait(&full_bar[s], (jw / SPW) & 1, p.err, p.wait_limit_ns);
+        const bool ready = !*abort_flag && mbar_wait(&full_bar[s], ph, p.err, p.wait_limit_ns);
+        if (++js == SPW) {
+          js = 0;
+          ph ^= 1u;
+        }
         if (!__all_sync(0xffffffffu, ready)) {
           *abort_flag = 1;
           break;
