@@ -338,7 +338,8 @@ pkv_status pkv_decode_step_host(const void* h_q, const void* h_k_new, const void
  * PKV_ERR_OOB) and re-quantise rows 0..slot % 16 of that block: the old codes
  * are decoded in float32 as min + ((q * (max - min)) / 255), min / max are
  * taken again over those rows and the new one, and all of them are encoded
- * again.  The tokens of one call must lie in distinct blocks.
+ * again.  The tokens of one call must lie in distinct blocks; k_cache, v_cache
+ * and slab_params must be 16-byte aligned (PKV_ERR_INVALID_ARG otherwise).
  * pkv_paged_decode_attention_int8: pkv_paged_decode_attention over such a
  * cache; dequantisation happens in registers as k_min sum(q) + dk (q . codes)
  * per score and v_min sum(p) + dv (p . codes) per output.  q_dtype is the type

@@ -348,9 +348,23 @@ extern "C" pkv_status pkv_paged_decode_step_int8(const void* q, const void* k_ne
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
-  if (!k_new || !v_new || !k_cache || !v_cache || !slab_params || !block_tables || !context_lens ||
-      (reinterpret_cast<uintptr_t>(slab_params) & 15u))
+  if (!k_new || !v_new || !k_cache || !v_cache || !slab_params || !block_tables || !context_lens || !q || !out ||
+      !workspace ||
+      ((reinterpret_cast<uintptr_t>(slab_params) | reinterpret_cast<uintptr_t>(k_cache) |
+        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+        reinterpret_cast<uintptr_t>(workspace)) & 15u))
     return PKV_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads || max_context_len < 0 || partition_tokens < 0 ||
+      partition_tokens % kBlockSize || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  {
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                   max_context_len, partition_tokens);
+    if (need == 0) return PKV_ERR_CUDA;
+    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  }
   const pkv_status st = launch_append_int8_step(k_new, v_new, k_cache, v_cache, slab_params, block_tables,
                                                 context_lens, batch, max_blocks_per_seq, num_blocks, num_kv_heads,
                                                 head_dim, q_dtype, slot_mapping_out, err_flag,

@@ -269,7 +269,8 @@ extern "C" pkv_status pkv_kv_append_int8(const void* k_new, const void* v_new, c
   if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !slab_params ||
-      (reinterpret_cast<uintptr_t>(slab_params) & 15u))
+      ((reinterpret_cast<uintptr_t>(slab_params) | reinterpret_cast<uintptr_t>(k_cache) |
+        reinterpret_cast<uintptr_t>(v_cache)) & 15u))
     return PKV_ERR_INVALID_ARG;
   if (num_tokens * num_kv_heads > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   auto kern = in_dtype == PKV_F16 ? append_int8_kernel<F16, false> : append_int8_kernel<BF16, false>;

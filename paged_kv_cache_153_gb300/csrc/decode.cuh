@@ -164,8 +164,8 @@ __device__ __forceinline__ int64_t part_range_of(int64_t f, int64_t W, int64_t R
 // range r of R owns the blocks with floor(r V / R) <= pos < floor((r+1) V / R).
 constexpr int kBlockCost = 4;
 
-// batches up to this size: the combine kernel sums the block counts itself
-// (each of its thread blocks reads every context length once)
+// batches up to this size: the narrow combine sums the block counts itself
+// (each of its warps reads every context length once)
 constexpr int kCombineLocalPrefix = 256;
 
 __device__ __forceinline__ int64_t seq_cost(const int* cum, const int* ne, int b, int Hkv, int A) {
@@ -1400,90 +1400,50 @@ __device__ __forceinline__ int64_t combine_slot(const CombineSpan& s, int64_t r)
 }
 
 // ---------------------------------------------------------------------------
-// combine: out[b, g*G + h] = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r over
-// the partial slots of (b, g); zeros for an empty context.  One thread block
-// per (b, g).  Each group of kSplit adjacent lanes owns 4 consecutive outputs;
-// lane s of the group merges pieces s, s + kSplit, ... (loads issued 4 at a
-// time), then the group combines its states with xor shuffles.  (b, g) pairs
-// written directly by the decode kernel are skipped.
+// The wide combine, for pairs split into many pieces (the partition split of
+// long contexts): out[b, g*G + h] = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M)
+// l_r over the partial slots of (b, g); zeros for an empty context.  One
+// thread block per (b, g).  Each group of kSplit adjacent lanes owns 4
+// consecutive outputs; lane s of the group merges pieces s, s + kSplit, ...
+// (loads issued 4 at a time), then the group combines its states with xor
+// shuffles.  (b, g) pairs written directly by the decode kernel are skipped.
+// Up to 8 lanes per output quad and at most 512 threads: a thread block of
+// 1024 threads at 64 registers holds a whole SM's register file, and the
+// 256 pairs of a 32-sequence batch then ran in two waves (the combine took
+// 10.6 us of a 90.7 us long-context FP8 step on GB300).
 // ---------------------------------------------------------------------------
-// WIDE: up to 8 lanes per output quad, at most 512 threads, for (sequence,
-// KV head) pairs split into many pieces; else one lane per quad.  (A thread
-// block of 1024 threads at 64 registers holds a whole SM's register file:
-// the 256 pairs of a 32-sequence batch then ran in two waves, and the
-// combine took 10.6 us of a 90.7 us long-context FP8 step on GB300.)
-template <int D, int G, bool WIDE>
+template <int D, int G>
 __host__ __device__ constexpr int combine_split() {
-  return !WIDE ? 1 : (512 / (G * D / 4) >= 8 ? 8 : 512 / (G * D / 4) >= 1 ? 512 / (G * D / 4) : 1);
+  return 512 / (G * D / 4) >= 8 ? 8 : 512 / (G * D / 4) >= 1 ? 512 / (G * D / 4) : 1;
 }
-template <int D, int G, bool WIDE>
+template <int D, int G>
 __host__ __device__ constexpr int combine_threads() {
-  return (G * D / 4) * combine_split<D, G, WIDE>() < 32 ? 32 : (G * D / 4) * combine_split<D, G, WIDE>();
+  return (G * D / 4) * combine_split<D, G>() < 32 ? 32 : (G * D / 4) * combine_split<D, G>();
 }
 
-template <typename QT, int D, int G, bool WIDE>
-__global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
-    paged_decode_combine_kernel(const __grid_constant__ DecodeParams p, int grid_ranges) {
-  constexpr int kSplit = combine_split<D, G, WIDE>();
+template <typename QT, int D, int G>
+__global__ void __launch_bounds__(combine_threads<D, G>())
+    paged_decode_combine_wide_kernel(const __grid_constant__ DecodeParams p, int grid_ranges) {
+  constexpr int kSplit = combine_split<D, G>();
   const int u = blockIdx.x;
   const int b = u / p.n_kv_heads, g = u % p.n_kv_heads;
   const int t = threadIdx.x / kSplit, sub = threadIdx.x % kSplit;
   const bool live_t = t < G * D / 4;
   auto* out = static_cast<typename QT::storage*>(p.out);
-  // Geometry: blocks and non-empty sequences before b and in all, and the
-  // blocks of b.  For a small batch and the narrow form (small thread blocks,
-  // which become resident beside the decode grid) they are summed here from
-  // the context lengths -- an input the decode kernel does not write -- while
-  // the decode grid still runs (this launch overlaps it), clamped exactly as
-  // the decode kernel clamps them; only the partials are then read after the
-  // wait.  Otherwise the prefixes the decode kernel leaves in the workspace
-  // are read after the wait.
-  //   The next launch is released at once (combine_early), or after the
-  // wait below: it is the next step's decode kernel (or INT8 append), which
-  // reads only inputs before its own wait and writes -- the cache, the
-  // workspace, the outputs -- only after it, that is after this grid (and so
-  // the decode grid before it) has completed.
+  // The next launch is released at once (combine_early), or after the wait
+  // below: it is the next step's decode kernel (or INT8 append), which reads
+  // only inputs before its own wait and writes -- the cache, the workspace,
+  // the outputs -- only after it, that is after this grid (and so the decode
+  // grid before it) has completed.  The geometry (blocks and non-empty
+  // sequences before b and in all, the blocks of b) is read after the wait
+  // from the prefixes the decode kernel leaves in the workspace.
   if (p.combine_early) pdl_release();
-  int64_t c0, ne_b, tot, tot_ne;
-  int nb;
-  if (!WIDE && p.batch <= kCombineLocalPrefix) {
-    __shared__ long long red[5][32];      // per-warp sums (up to 32 warps)
-    long long v[5] = {0, 0, 0, 0, 0};
-    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
-      const int ctx = p.context_lens[i];
-      const int n = ctx < 0 ? 0 : min((ctx + kBlockSize - 1) / kBlockSize, min(p.max_blocks_per_seq, p.max_nblk));
-      v[2] += n;
-      v[3] += n > 0;
-      if (i < b) {
-        v[0] += n;
-        v[1] += n > 0;
-      }
-      if (i == b) v[4] = n;
-    }
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
-      if (lane == 0) red[k][wid] = v[k];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-      v[k] = 0;
-      for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) v[k] += red[k][w2];
-    }
-    c0 = v[0], ne_b = v[1], tot = v[2], tot_ne = v[3];
-    nb = static_cast<int>(v[4]);
-    pdl_wait_and_release();
-  } else {
-    pdl_wait_and_release();
-    c0 = p.ws_cum[b];
-    nb = p.ws_cum[b + 1] - p.ws_cum[b];
-    tot = p.ws_cum[p.batch];
-    ne_b = p.ws_cum[p.batch + 1 + b];
-    tot_ne = p.ws_cum[2 * p.batch + 1];
-  }
+  pdl_wait_and_release();
+  const int64_t c0 = p.ws_cum[b];
+  const int nb = p.ws_cum[b + 1] - p.ws_cum[b];
+  const int64_t tot = p.ws_cum[p.batch];
+  const int64_t ne_b = p.ws_cum[p.batch + 1 + b];
+  const int64_t tot_ne = p.ws_cum[2 * p.batch + 1];
   const int64_t base_out = (static_cast<int64_t>(b) * p.n_q_heads + g * G) * D + 4 * t;
   auto store4 = [&](float a, float b2, float c, float d) {
     const uint32_t lo = pack2(a, b2, QT{}), hi = pack2(c, d, QT{});
@@ -1498,7 +1458,7 @@ __global__ void __launch_bounds__(combine_threads<D, G, WIDE>())
   if (sp.r0 == sp.r1) return;   // one segment: written by the decode kernel
   const int h = live_t ? (4 * t) / D : 0, e = live_t ? (4 * t) % D : 0;
   float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
-  constexpr int kBatch = WIDE ? 4 : 8;   // partials whose loads are issued together, per lane
+  constexpr int kBatch = 4;   // partials whose loads are issued together, per lane
   for (int64_t rb = sp.r0 + sub; rb <= sp.r1; rb += kBatch * kSplit) {
     float2 ml[kBatch];
     float4 ov[kBatch];
@@ -1571,7 +1531,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   constexpr int kBatch = kQPL >= 8 ? 1 : kQPL >= 4 ? 2 : 4;   // pieces loaded together
   const int lane = threadIdx.x & 31;
   const int u = blockIdx.x * kCombineWarps + static_cast<int>(threadIdx.x >> 5);
-  // (release: as in paged_decode_combine_kernel)
+  // (release: as in paged_decode_combine_wide_kernel)
   if (p.combine_early) pdl_release();
   if (u >= p.batch * p.n_kv_heads) {
     pdl_wait();   // (every warp waits: this grid completes after the decode grid)

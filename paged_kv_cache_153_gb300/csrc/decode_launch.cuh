@@ -143,12 +143,12 @@ pkv_status launch_decode_variant(DecodeParams& p, LaunchInfo& li, cudaStream_t s
     // KV head) (one per range it meets): merge those with several lanes per output
     const bool wide = p.part_blocks > 0 && (p.max_nblk + p.part_blocks - 1) / p.part_blocks >= 16;
     const cudaError_t e =
-        wide ? launch_pdl(paged_decode_combine_kernel<QT, D, G, true>, dim3(units),
-                          dim3(combine_threads<D, G, true>()), 0, stream, p, grid)
+        wide ? launch_pdl(paged_decode_combine_wide_kernel<QT, D, G>, dim3(units),
+                          dim3(combine_threads<D, G>()), 0, stream, p, grid)
              : launch_pdl(paged_decode_combine_warps_kernel<QT, D, G>,
                           dim3((units + kCombineWarps - 1) / kCombineWarps), dim3(kCombineWarps * 32), 0, stream,
                           p, grid);
-    if (cuda_failed(e, "paged_decode_combine_kernel launch")) return PKV_ERR_CUDA;
+    if (cuda_failed(e, "combine kernel launch")) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }

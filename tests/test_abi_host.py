@@ -125,3 +125,24 @@ def test_host_pool_matches_oracle_pool(pkv, seed):
 def test_blocks_needed(pkv):
     for t in [0, 1, 15, 16, 17, 1200, 65536]:
         assert pkv.pkv_blocks_needed(t) == blocks_needed(t)
+
+
+def test_int8_step_validates_everything_before_its_first_launch(pkv):
+    # the INT8 step launches the re-quantising append before the decode, so
+    # every argument the decode would refuse is refused before the append
+    # writes the cache (no CUDA call is needed to see these)
+    lib = pkv.lib
+    a = C.c_void_p(4096)          # 16-byte aligned stand-in pointers
+    odd = C.c_void_p(4096 + 8)
+
+    def step(q=a, kc=a, vc=a, prm=a, out=a, ws=a, hq=32, hkv=8, part=0):
+        return lib.pkv_paged_decode_step_int8(q, a, a, kc, vc, prm, a, a, 4, hq, hkv, 128, 16, 8, 64, 128, 0.1,
+                                              out, 1, part, None, ws, 1 << 24, None, None)
+    assert step(kc=odd) == 1 and step(vc=odd) == 1 and step(prm=odd) == 1
+    assert step(q=None) == 1 and step(out=None) == 1 and step(ws=None) == 1
+    assert step(q=odd) == 1 and step(out=odd) == 1 and step(ws=odd) == 1
+    assert step(hq=30) == 1            # H_q not a multiple of H_kv
+    assert step(part=24) == 1          # partition not a multiple of the block size
+    assert step(hq=24) == 2            # group 3 is not built
+    # the plain INT8 append wants aligned caches as well
+    assert lib.pkv_kv_append_int8(a, a, a, 1, odd, a, a, 64, 8, 128, 16, 1, None, None) == 1
