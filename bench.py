@@ -71,7 +71,7 @@ def describe(w: wl.Workload) -> dict:
 
 
 # the sources each timed kernel is built from: a committed DRAM-traffic figure
-# stays valid while these files are unchanged
+# stays valid while the code of these files (comments and layout aside) is unchanged
 _COMMON_SOURCES = ("pkv_common.cuh", "host_util.h")
 _DECODE_SOURCES = ("api.cu", "decode.cuh", "decode_launch.cuh", "decode_f16.cu", "decode_bf16.cu",
                    "decode_e4m3.cu", "decode_e5m2.cu", "decode_int8.cu")
@@ -83,13 +83,40 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to
+    one space (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":                       # a literal: copy up to its closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):         # a line comment
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):         # a block comment
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest(family: str = "decode") -> str:
+    """Hash of the code (not the comments) of the sources a workload's kernels
+    are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_153_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[family]):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -421,14 +421,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   // wait_first).  Every global write (the new rows, slots,
   // outputs, partials, prefixes) is made by the consumer warps after their
   // wait for the previous kernel.
-  //   The combine kernel is released early: at once when it releases its
-  // own successor only after its wait (combine_early = 0).  Otherwise -- the
-  // combine releases the next step's decode, whose producer reads the cache
-  // before its wait, or the next step's INT8 append, which reads the slabs
-  // that this step's append writes before its own wait, at once -- at once
-  // too, unless this launch appends the step's new rows (fused step: once
-  // those cache writes are fenced) or waits for such an append (wait_first:
-  // at the first return from the wait).
+  //   When the combine is released.  With combine_early = 0 the combine
+  // releases its own successor only after its wait, and this kernel releases
+  // the combine at once.  With combine_early = 1 the combine releases the
+  // next step's kernel at once: the next decode, whose producer reads the
+  // cache before its wait, or the next INT8 append, which reads before its
+  // wait the slabs that this step's append wrote.  So this kernel then
+  // releases at once only if it neither appends the step's new rows (fused
+  // step: it releases once those cache writes are fenced) nor waits for such
+  // an append (wait_first: it releases at the first return from that wait).
   if (!p.combine_early || (p.k_new == nullptr && !p.wait_first)) pdl_release();
 
   // ---- 1. per-sequence block counts and their prefix (all threads) -------
