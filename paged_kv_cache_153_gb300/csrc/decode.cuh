@@ -494,74 +494,90 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
   }
   __syncthreads();
   const int64_t W = static_cast<int64_t>(Hkv) * cum[p.batch];
-  if (warp < NW) {
-    // the previous kernel has completed and its writes are visible (with
-    // wait_first, only thread block 0 waits here, for its prefixes; the
-    // others wait before their first output or partial)
-    if (!p.wait_first || blockIdx.x == 0) pdl_wait();
-    if (blockIdx.x == 0 && p.ws_cum != nullptr)
-      for (int b = tid; b <= p.batch; b += NW * 32) {
-        p.ws_cum[b] = cum[b];
-        p.ws_cum[p.batch + 1 + b] = ne[b];
-      }
-  }
 
   const int64_t R = gridDim.x;
   const int A = p.unit_cost;
   const int64_t V = seq_cost(cum, ne, p.batch, Hkv, A);   // balanced mode: total cost
 
-  // ---- 2. fused step: append the new rows (position ctx - 1) --------------
-  // The slot is computed from the block table here.  No thread block of this
-  // grid reads that slot from the cache: the consumer that processes the
-  // last block of (b, g) patches the row in shared memory instead (below).
-  // The consumer warps do the writes; the producer starts streaming at once.
-  // Chunks are dealt to thread blocks first (chunk c to block c mod grid), so
-  // every block carries an equal share of this start-up work.
+  // ---- 2. the consumers' first global writes ------------------------------
+  // They follow the wait for the previous kernel (whose completion makes its
+  // writes visible) and come just before a consumer group's first output or
+  // partial, or at its end: until then the consumers only compute from the
+  // staged blocks, while the previous kernel finishes.  They are the
+  // prefixes for the combine (thread block 0) and, in the fused step, the
+  // new rows (position ctx - 1).  The slot is computed from the block table
+  // here.  No thread block of this grid reads that slot from the cache: the
+  // consumer that processes the last block of (b, g) patches the row in
+  // shared memory instead (below).  Chunks of the new rows are dealt to
+  // thread blocks first (chunk c to block c mod grid), so every block carries
+  // an equal share.  Called by all consumer threads together (a named
+  // barrier inside).
   using NT = std::conditional_t<T::kEsz == 1, QT, KV>;   // element type of the new rows
-  if (p.k_new != nullptr && warp < NW) {
-    constexpr int kChunks = D / 8;                           // 8 input elements per chunk
-    const int64_t total = 2ll * p.batch * Hkv * kChunks;
-    for (int64_t idx = static_cast<int64_t>(tid) * gridDim.x + blockIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * (NW * 32)) {
-      int64_t x = idx;
-      const int c = static_cast<int>(x % kChunks);
-      x /= kChunks;
-      const int g = static_cast<int>(x % Hkv);
-      x /= Hkv;
-      const int b = static_cast<int>(x % p.batch);
-      const bool is_v = x >= p.batch;
-      const bool reports = !is_v && g == 0 && c == 0 && p.slots_out != nullptr;   // one thread per sequence
-      // the new row's chunk is loaded before the table entry, so both loads are in flight together
-      const unsigned char* src = static_cast<const unsigned char*>(is_v ? p.v_new : p.k_new) +
-                                 ((static_cast<int64_t>(b) * Hkv + g) * D + 8 * c) * 2;
-      const uint4 raw = *reinterpret_cast<const uint4*>(src);
-      const int n = ntok[b];
-      if (n == 0) {
-        if (reports) p.slots_out[b] = -1;   // nothing appended (as the slot mapping reports padding)
-        continue;
+  bool writes_done = false;
+  auto first_writes = [&]() {
+    if (writes_done) return;
+    writes_done = true;
+    pdl_wait();
+    if (blockIdx.x == 0 && p.ws_cum != nullptr)
+      for (int b = tid; b <= p.batch; b += NW * 32) {
+        p.ws_cum[b] = cum[b];
+        p.ws_cum[p.batch + 1 + b] = ne[b];
       }
-      const int pos = n - 1;
-      const int32_t blk = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + pos / kBlockSize];
-      if (blk < 0 || blk >= p.num_blocks) {
-        record_error(p.err, PKV_ERR_OOB);
-        if (reports) p.slots_out[b] = -1;
-        continue;
+    if (p.k_new != nullptr) {
+      constexpr int kChunks = D / 8;                           // 8 input elements per chunk
+      const int64_t total = 2ll * p.batch * Hkv * kChunks;
+      for (int64_t idx = static_cast<int64_t>(tid) * gridDim.x + blockIdx.x; idx < total;
+           idx += static_cast<int64_t>(gridDim.x) * (NW * 32)) {
+        int64_t x = idx;
+        const int c = static_cast<int>(x % kChunks);
+        x /= kChunks;
+        const int g = static_cast<int>(x % Hkv);
+        x /= Hkv;
+        const int b = static_cast<int>(x % p.batch);
+        const bool is_v = x >= p.batch;
+        const bool reports = !is_v && g == 0 && c == 0 && p.slots_out != nullptr;   // one thread per sequence
+        // the new row's chunk is loaded before the table entry, so both loads are in flight together
+        const unsigned char* src = static_cast<const unsigned char*>(is_v ? p.v_new : p.k_new) +
+                                   ((static_cast<int64_t>(b) * Hkv + g) * D + 8 * c) * 2;
+        const uint4 raw = *reinterpret_cast<const uint4*>(src);
+        const int n = ntok[b];
+        if (n == 0) {
+          if (reports) p.slots_out[b] = -1;   // nothing appended (as the slot mapping reports padding)
+          continue;
+        }
+        const int pos = n - 1;
+        const int32_t blk = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + pos / kBlockSize];
+        if (blk < 0 || blk >= p.num_blocks) {
+          record_error(p.err, PKV_ERR_OOB);
+          if (reports) p.slots_out[b] = -1;
+          continue;
+        }
+        const int64_t row = (static_cast<int64_t>(blk) * p.block_heads + g) * kBlockSize + pos % kBlockSize;
+        if (reports) p.slots_out[b] = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
+        unsigned char* dst =
+            static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache)) + (row * D + 8 * c) * T::kEsz;
+        if constexpr (T::kEsz == 2)
+          *reinterpret_cast<uint4*>(dst) = raw;
+        else if constexpr (!std::is_same<KV, U8>::value)   // (an INT8 cache has no fused append)
+          *reinterpret_cast<uint2*>(dst) = quant8_fp8<KV>(&raw, is_v ? scales[Hkv + g] : scales[g], NT{});
       }
-      const int64_t row = (static_cast<int64_t>(blk) * p.block_heads + g) * kBlockSize + pos % kBlockSize;
-      if (reports) p.slots_out[b] = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
-      unsigned char* dst =
-          static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache)) + (row * D + 8 * c) * T::kEsz;
-      if constexpr (T::kEsz == 2)
-        *reinterpret_cast<uint4*>(dst) = raw;
-      else if constexpr (!std::is_same<KV, U8>::value)   // (an INT8 cache has no fused append)
-        *reinterpret_cast<uint2*>(dst) = quant8_fp8<KV>(&raw, is_v ? scales[Hkv + g] : scales[g], NT{});
+      // every consumer's rows are in memory before any thread releases the
+      // combine (the first release of a thread block counts for all of it;
+      // the producer warp never releases)
+      __threadfence();
+      named_bar_sync(1, NW * 32);
+      pdl_release();
+    } else if (p.wait_first) {
+      pdl_release();
     }
-    // every consumer's rows are in memory before any thread releases the
-    // combine (the first release of a thread block counts for all of it; the
-    // producer warp never releases)
-    __threadfence();
-    named_bar_sync(1, NW * 32);
-    pdl_release();
+  };
+  // The CUDA-core consumer defers these writes as described (on the 16-way
+  // MHA batch: 151.3 against 156.5 us per step on GB300).  The tensor-core
+  // consumer makes them at once: its first segment is often most of its
+  // range, and deferring the combine's release that long measured slower
+  // (64-sequence GQA 76.1 against 74.4 us, shared prefix 24.7 against 20.9).
+  if constexpr (MMA) {
+    if (warp < NW) first_writes();
   }
 
   if (warp == NW) {
@@ -1311,7 +1327,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
     }
 
     // ---- merge the NW warps' states and write the result ---------------------
-    if (p.wait_first) pdl_wait_and_release();   // (before the first global write; at once afterwards)
+    first_writes();
     named_bar_sync(1, NW * 32);
     const float vscale = scales[Hkv + d.g];
     for (int idx = tid; idx < G * D; idx += NW * 32) {
@@ -1344,6 +1360,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, MMA ? 3 : 1) paged_decode_kerne
     named_bar_sync(1, NW * 32);
     ++j;
   }
+  first_writes();   // (a consumer group that wrote nothing: the wait, prefixes and new rows)
 }
 
 // ---------------------------------------------------------------------------
