@@ -1,6 +1,7 @@
 """bench.py's record of which sources each timed kernel is built from: a
-committed DRAM-traffic figure is reported only while those files are
-unchanged, so every kernel source must belong to some family."""
+committed DRAM-traffic figure is reported only while the code of those files
+(comments and layout aside) is unchanged, so every kernel source must belong
+to some family."""
 import os
 
 import bench
@@ -30,3 +31,12 @@ def test_digest_depends_only_on_its_family():
         d = bench.kernel_source_digest(fam)
         assert len(d) == 16 and d == bench.kernel_source_digest(fam)
     assert len({bench.kernel_source_digest(f) for f in bench.KERNEL_SOURCES}) == len(bench.KERNEL_SOURCES)
+
+
+def test_code_only_drops_comments_and_layout_but_keeps_literals():
+    src = 'int a = 1; // note\n/* block\n comment */  int  b = 2;\nasm("x // y; /* z */");\nchar c = \'/\';'
+    assert bench.code_only(src) == 'int a = 1; int b = 2; asm("x // y; /* z */"); char c = \'/\';'
+    # a comment edit leaves the code as it was; a code edit does not
+    assert bench.code_only("x = 1; // one") == bench.code_only("x = 1;   // another\n")
+    assert bench.code_only("x = 1;") != bench.code_only("x = 2;")
+    assert bench.code_only('s = "a\\"//b";') == 's = "a\\"//b";'
