@@ -32,12 +32,15 @@
 //
 // Consumers.  Scores are kept in the log2 domain (scale * log2(e) applied in
 // fp32), so exponentials are exp2.
-//  * CUDA-core consumer (G = 1; FP8 with 64-byte rows): a token row is split over
+//  * CUDA-core consumer (G = 1 on 16-bit and FP8 caches; one-byte caches with
+//    64-byte rows): a token row is split over
 //    LPT = D / 8 lanes; partial dot products are reduced by a butterfly
 //    reduce-scatter; p is shared through a per-warp scratch row; p.V
 //    accumulates in fp32 registers, each lane owning 8 output elements.
-//  * Tensor-core consumer (G >= 2; 16-bit cache, or FP8 with 128-byte rows
-//    converted to f16 in registers): q.K^T of a block is one
+//  * Tensor-core consumer (G >= 2 on a 16-bit cache or an FP8 cache with
+//    128-byte rows, converted to f16 in registers; an INT8 cache with 128-byte
+//    rows at every G, its codes entering the MMAs as 1024 + code with the
+//    affine terms applied per block): q.K^T of a block is one
 //    mma.m16n8k16 per 16 head_dim elements with the 16 tokens as M and the G
 //    query heads (zero-padded to 8) as N; the fp32 scores of the C fragment
 //    go through the online softmax in registers; p is rounded to the cache's
@@ -48,10 +51,11 @@
 //    normaliser l sums exactly the p that is multiplied.
 //
 // Fused step (k_new != null).  The same launch also appends each sequence's
-// new K/V row at position ctx - 1: thread blocks share the global writes in
-// their prologue (slots from the block table), and the consumer of the last
-// block of every (sequence, KV head) overwrites that row of its staged block
-// with the new row, so no block of the grid depends on another's write.
+// new K/V row at position ctx - 1: the consumer warps of all thread blocks
+// share these global writes (slots from the block table) after their wait for
+// the previous kernel, and the consumer of the last block of every (sequence,
+// KV head) overwrites that row of its staged block with the new row, so no
+// block of the grid depends on another's write.
 #pragma once
 
 #include <cuda.h>
